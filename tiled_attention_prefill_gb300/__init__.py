@@ -1,0 +1,15 @@
+"""Fused, tiled self-attention forward (prefill) for NVIDIA GB300 (sm_103a).
+
+``forward`` and the other entry points live in :mod:`.fa` (a thin ctypes
+binding over the C-ABI library ``libfa_gb300.so``); importing this package
+does not load the library.
+"""
+
+__version__ = "0.1.0"
+
+
+def __getattr__(name):
+    if name in ("forward", "fa", "load_library", "FAError"):
+        from . import fa as _fa
+        return _fa if name == "fa" else getattr(_fa, name)
+    raise AttributeError(name)
