@@ -1,0 +1,110 @@
+"""The C-ABI library: it loads, exports what include/fa.h declares, and rejects bad
+arguments on the host (these calls return before any CUDA work, so they run without a GPU)."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tiled_attention_prefill_gb300 import _build, fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    assert declared_functions() == sorted(fa.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_error_strings(lib):
+    assert lib.fa_version() == 100
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        s = lib.fa_error_string(code).decode()
+        assert s and s != "unknown error code"
+    assert lib.fa_error_string(12345).decode() == "unknown error code"
+
+
+def test_watchdog_setter(lib):
+    assert lib.fa_set_watchdog_ns(0) == fa.FA_OK
+
+
+def _call(lib, q=16, k=32, v=48, o=1 << 40, lse=0, B=1, H=1, N=8, D=64, scale=0.125, causal=0, dtype=0):
+    return lib.fa_forward(q or None, k or None, v or None, o or None, lse or None, B, H, N, D, scale, causal, dtype,
+                          None)
+
+
+def test_null_pointers_rejected(lib):
+    assert _call(lib, q=0) == fa.FA_ERR_INVALID_ARG
+    assert _call(lib, k=0) == fa.FA_ERR_INVALID_ARG
+    assert _call(lib, v=0) == fa.FA_ERR_INVALID_ARG
+    assert _call(lib, o=0) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field", ["B", "H", "N"])
+@pytest.mark.parametrize("value", [0, -3])
+def test_nonpositive_sizes_rejected(lib, field, value):
+    assert _call(lib, **{field: value}) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("D", [0, 32, 96, 256])
+def test_unsupported_head_dim(lib, D):
+    assert _call(lib, D=D) == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype", [-1, 2, 7])
+def test_unsupported_dtype(lib, dtype):
+    assert _call(lib, dtype=dtype) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_misaligned_pointers(lib):
+    assert _call(lib, q=18) == fa.FA_ERR_ALIGN
+    assert _call(lib, k=40) == fa.FA_ERR_ALIGN
+    assert _call(lib, v=8) == fa.FA_ERR_ALIGN
+    assert _call(lib, o=(1 << 40) + 4) == fa.FA_ERR_ALIGN
+    assert _call(lib, lse=(1 << 41) + 2) == fa.FA_ERR_ALIGN
+
+
+def test_too_large(lib):
+    assert _call(lib, N=(1 << 30) + 1) == fa.FA_ERR_TOO_LARGE
+    assert _call(lib, B=1 << 16, H=1 << 16, N=256) == fa.FA_ERR_TOO_LARGE
+
+
+def test_output_aliasing_rejected(lib):
+    base = 1 << 40
+    n_bytes = 1 * 1 * 8 * 64 * 2
+    assert _call(lib, q=base, k=base + 4096, v=base + 8192, o=base + 16) == fa.FA_ERR_INVALID_ARG
+    o = base + (1 << 20)
+    assert _call(lib, q=base, k=base + 4096, v=base + 8192, o=o, lse=o + n_bytes - 4) == fa.FA_ERR_INVALID_ARG
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        fa.forward(x, x, x)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(ImportError):
+        fa.load_library(str(tmp_path / "libmissing.so"))
+    assert isinstance(ctypes.CDLL, type)

@@ -1,0 +1,160 @@
+"""GPU parity: the CUDA path (through the C-ABI binding) against the fp64 oracle.
+
+Tolerances (max abs error over all compared elements): O within 2e-3 for fp16 I/O
+and 1e-2 for bf16 I/O, LSE within 1e-3.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tiled_attention_prefill_gb300 import fa, workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = {"fp16": 2e-3, "bf16": 1e-2}
+TOL_LSE = 1e-3
+
+
+def run_cuda(q, k, v, causal, scale, lse=True):
+    o, l = fa.forward(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale, return_lse=lse)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    o64 = o.float().cpu().numpy().astype(np.float64)
+    l64 = l.cpu().numpy().astype(np.float64) if l is not None else None
+    return o64, l64
+
+
+def assert_close(o, lse, ro, rl, dtype, what=""):
+    assert np.isfinite(o).all(), "non-finite O " + what
+    err_o = np.abs(o - ro)
+    i = np.unravel_index(np.argmax(err_o), err_o.shape)
+    assert err_o.max() <= TOL_O[dtype], "O %s: max err %.3e at %s (got %r want %r)" % (
+        what, err_o.max(), i, o[i], ro[i])
+    if lse is not None:
+        assert np.isfinite(lse).all(), "non-finite LSE " + what
+        err_l = np.abs(lse - rl)
+        j = np.unravel_index(np.argmax(err_l), err_l.shape)
+        assert err_l.max() <= TOL_LSE, "LSE %s: max err %.3e at %s" % (what, err_l.max(), j)
+
+
+SMALL_SHAPES = [
+    (1, 1, 1, 64), (1, 1, 2, 128), (1, 2, 17, 64), (1, 1, 127, 128), (1, 1, 128, 64), (1, 1, 129, 128),
+    (2, 3, 200, 64), (1, 2, 256, 128), (1, 1, 257, 64), (1, 2, 384, 128), (1, 1, 513, 64), (1, 1, 1000, 128),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_small_shapes_against_oracle(shape, dtype, causal):
+    B, H, N, D = shape
+    w = workloads.Workload("t", B, H, N, D, dtype, causal, seed=7 * N + D + B)
+    q, k, v = workloads.make_qkv(w)
+    o, lse = run_cuda(q, k, v, causal, w.scale)
+    ro, rl = oracle.attention(q, k, v, w.scale, causal)
+    assert_close(o, lse, ro, rl, dtype, str(shape))
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c3c"])
+def test_workload_full_oracle(name):
+    """Every output element of the smaller workloads against the oracle."""
+    w = workloads.WORKLOADS[name]
+    q, k, v = workloads.make_qkv(w)
+    o, lse = run_cuda(q, k, v, w.causal, w.scale)
+    ro, rl = oracle.attention(q, k, v, w.scale, w.causal)
+    assert_close(o, lse, ro, rl, w.dtype, name)
+
+
+def sample_rows(w, n_heads=6, seed=0):
+    """(bh, i) pairs: tile edges, the first and last rows, and random rows of a few heads."""
+    rng = np.random.default_rng(seed)
+    BH, N = w.B * w.H, w.N
+    heads = sorted(set([0, BH - 1] + list(rng.integers(0, BH, size=n_heads))))
+    fixed = [0, 1, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1]
+    rows = []
+    for bh in heads:
+        idx = set(i for i in fixed if 0 <= i < N) | set(rng.integers(0, N, size=24).tolist())
+        rows += [(bh, i) for i in sorted(idx)]
+    return np.array(rows, dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["c4", "c5"])
+def test_workload_sampled_rows(name):
+    """Full-size workloads: every output is finite; sampled rows match the oracle."""
+    w = workloads.WORKLOADS[name]
+    q, k, v = workloads.make_qkv(w)
+    o, lse = run_cuda(q, k, v, w.causal, w.scale)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    rows = sample_rows(w)
+    ro, rl = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
+    o_s = o.reshape(-1, w.N, w.D)[rows[:, 0], rows[:, 1]]
+    l_s = lse.reshape(-1, w.N)[rows[:, 0], rows[:, 1]]
+    assert_close(o_s, l_s, ro, rl, w.dtype, name)
+
+
+def test_lse_optional():
+    w = workloads.WORKLOADS["c1"]
+    q, k, v = workloads.make_qkv(w)
+    o, lse = run_cuda(q, k, v, False, w.scale, lse=False)
+    assert lse is None
+    ro, _ = oracle.attention(q, k, v, w.scale, False)
+    assert_close(o, None, ro, None, "fp16", "no-lse")
+
+
+def test_default_scale():
+    w = workloads.WORKLOADS["c1"].with_(D=128)
+    q, k, v = workloads.make_qkv(w)
+    o, lse = run_cuda(q, k, v, True, None)
+    ro, rl = oracle.attention(q, k, v, 1.0 / np.sqrt(128.0), True)
+    assert_close(o, lse, ro, rl, "fp16", "default scale")
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_no_writes_outside_outputs(dtype):
+    """Guard regions around O and LSE keep their sentinel values (out-of-bounds write check)."""
+    w = workloads.Workload("g", 1, 3, 333, 128, dtype, True, seed=99)
+    q, k, v = (x.cuda() for x in workloads.make_qkv(w))
+    pad = 4096
+    numel = q.numel()
+    o_big = torch.full((numel + 2 * pad,), 7.0, dtype=q.dtype, device="cuda")
+    l_big = torch.full((w.B * w.H * w.N + 2 * pad,), -3.0, dtype=torch.float32, device="cuda")
+    o = o_big[pad:pad + numel].view(q.shape)
+    lse = l_big[pad:pad + w.B * w.H * w.N].view(w.B, w.H, w.N)
+    fa.forward(q, k, v, causal=True, scale=w.scale, out=o, lse=lse)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    assert bool((o_big[:pad] == 7.0).all()) and bool((o_big[pad + numel:] == 7.0).all())
+    assert bool((l_big[:pad] == -3.0).all()) and bool((l_big[pad + w.B * w.H * w.N:] == -3.0).all())
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, True)
+    assert_close(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ro, rl, dtype)
+
+
+def test_bitwise_deterministic():
+    w = workloads.WORKLOADS["c3c"]
+    q, k, v = (x.cuda() for x in workloads.make_qkv(w))
+    o1, l1 = fa.forward(q, k, v, causal=True, scale=w.scale)
+    o2, l2 = fa.forward(q, k, v, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_errors_surface_as_exceptions():
+    x = torch.zeros(1, 1, 8, 96, dtype=torch.float16, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        fa.forward(x, x, x)
+    assert e.value.code == fa.FA_ERR_UNSUPPORTED
+
+
+def test_runs_on_a_side_stream():
+    w = workloads.WORKLOADS["c1"].with_(H=4, N=700)
+    q, k, v = (x.cuda() for x in workloads.make_qkv(w))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = fa.forward(q, k, v, causal=False, scale=w.scale)
+    s.synchronize()
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, False)
+    assert_close(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ro, rl, "fp16")

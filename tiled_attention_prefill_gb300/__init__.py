@@ -5,11 +5,12 @@ binding over the C-ABI library ``libfa_gb300.so``); importing this package
 does not load the library.
 """
 
+import importlib
+
 __version__ = "0.1.0"
 
 
 def __getattr__(name):
-    if name in ("forward", "fa", "load_library", "FAError"):
-        from . import fa as _fa
-        return _fa if name == "fa" else getattr(_fa, name)
+    if name in ("forward", "load_library", "FAError", "check_device_status"):
+        return getattr(importlib.import_module(__name__ + ".fa"), name)
     raise AttributeError(name)

@@ -1,0 +1,215 @@
+// C-ABI entry points: argument validation, TMA descriptor encoding, kernel selection.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_launch.cuh"
+
+namespace fa {
+
+FA_DECLARE_LAUNCH(extern, 64, false, false)
+FA_DECLARE_LAUNCH(extern, 64, false, true)
+FA_DECLARE_LAUNCH(extern, 64, true, false)
+FA_DECLARE_LAUNCH(extern, 64, true, true)
+FA_DECLARE_LAUNCH(extern, 128, false, false)
+FA_DECLARE_LAUNCH(extern, 128, false, true)
+FA_DECLARE_LAUNCH(extern, 128, true, false)
+FA_DECLARE_LAUNCH(extern, 128, true, true)
+
+// Error bits OR-ed in by kernels of this library on the device they ran on.
+__device__ unsigned int g_device_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+constexpr long long kL2SectionBytes = 32ll << 20;  // K+V bytes of the heads kept close in time
+
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+thread_local int t_last_cuda_error = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceInfo {
+  bool ready = false;
+  int status = FA_OK;  // FA_OK or FA_ERR_UNSUPPORTED
+  int num_sms = 0;
+  unsigned int* status_word = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return FA_ERR_CUDA;
+}
+
+// One-time per-device setup: architecture check, SM count, status word, driver entry point.
+int device_setup(int dev, DeviceInfo*& out) {
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    d.status = (major == 10 && minor == 3) ? FA_OK : FA_ERR_UNSUPPORTED;
+    if (d.status == FA_OK) {
+      void* sym = nullptr;
+      e = cudaGetSymbolAddress(&sym, g_device_status);
+      if (e != cudaSuccess) return cuda_fail(e);
+      d.status_word = static_cast<unsigned int*>(sym);
+    }
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cuda_fail(cudaErrorSymbolNotFound);
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.ready = true;
+  }
+  out = &d;
+  return d.status;
+}
+
+// [BH, N, D] 16-bit tensor viewed as 3-D (D, N, BH); box (64, box_rows, 1), 128-byte swizzle,
+// zero fill outside the tensor.
+int encode_map(CUtensorMap* map, const void* base, bool bf16, int BH, int N, int D, int box_rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return FA_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_error_string(int code) {
+  switch (code) {
+    case FA_OK: return "success";
+    case FA_ERR_INVALID_ARG: return "invalid argument (null pointer, non-positive size, or aliasing output)";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration (D must be 64 or 128, dtype fp16/bf16, device sm_103)";
+    case FA_ERR_ALIGN: return "misaligned pointer (Q/K/V/O need 16-byte alignment, LSE 4-byte)";
+    case FA_ERR_CUDA: return "CUDA call failed (see fa_last_cuda_error)";
+    case FA_ERR_TIMEOUT: return "device-side wait exceeded the watchdog limit";
+    case FA_ERR_TOO_LARGE: return "sizes exceed the supported index range";
+    default: return "unknown error code";
+  }
+}
+
+int fa_last_cuda_error(void) { return fa::t_last_cuda_error; }
+
+int fa_set_watchdog_ns(unsigned long long ns) {
+  fa::g_timeout_ns.store(ns == 0 ? fa::kDefaultTimeoutNs : ns);
+  return FA_OK;
+}
+
+int fa_check_device_status(void) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fa::cuda_fail(e);
+  fa::DeviceInfo* d = nullptr;
+  int rc = fa::device_setup(dev, d);
+  if (rc != FA_OK) return rc;
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fa::cuda_fail(e);
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, fa::g_device_status, sizeof(word));
+  if (e != cudaSuccess) return fa::cuda_fail(e);
+  if (word != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(fa::g_device_status, &zero, sizeof(zero));
+    if (e != cudaSuccess) return fa::cuda_fail(e);
+  }
+  return (word & fa::kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+               float scale, int causal, int dtype, void* stream) {
+  using namespace fa;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+  auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+  if (mis16(q) || mis16(k) || mis16(v) || mis16(o)) return FA_ERR_ALIGN;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
+
+  const long long BH = static_cast<long long>(B) * H;
+  const long long num_mb = (static_cast<long long>(N) + kItemRows - 1) / kItemRows;
+  if (N > (1 << 30) || BH > 0x7fffffffll || BH * num_mb > 0x7fffffffll) return FA_ERR_TOO_LARGE;
+  const size_t tensor_bytes = static_cast<size_t>(BH) * N * D * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH) * N * sizeof(float);
+  if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
+      overlaps(o, tensor_bytes, v, tensor_bytes) || (lse && overlaps(o, tensor_bytes, lse, lse_bytes)))
+    return FA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DeviceInfo* info = nullptr;
+  int rc = device_setup(dev, info);
+  if (rc != FA_OK) return rc;
+
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
+
+  Params p{};
+  if ((rc = encode_map(&p.tm_q, q, bf16, static_cast<int>(BH), N, D, kBM)) != FA_OK) return rc;
+  if ((rc = encode_map(&p.tm_k, k, bf16, static_cast<int>(BH), N, D, kBN)) != FA_OK) return rc;
+  if ((rc = encode_map(&p.tm_v, v, bf16, static_cast<int>(BH), N, D, kBN)) != FA_OK) return rc;
+  if ((rc = encode_map(&p.tm_o, o, bf16, static_cast<int>(BH), N, D, 32)) != FA_OK) return rc;
+  p.lse = lse;
+  p.status = info->status_word;
+  p.timeout_ns = g_timeout_ns.load();
+  p.BH = static_cast<int>(BH);
+  p.N = N;
+  p.num_mb = static_cast<int>(num_mb);
+  p.num_items = static_cast<int>(BH * num_mb);
+  const long long kv_head_bytes = 2ll * N * D * 2;
+  long long section = kL2SectionBytes / (kv_head_bytes > 0 ? kv_head_bytes : 1);
+  p.section = static_cast<int>(section < 1 ? 1 : (section > BH ? BH : section));
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+  const int grid = p.num_items < info->num_sms ? p.num_items : info->num_sms;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool c = causal != 0;
+  if (D == 64) {
+    if (!bf16) e = c ? launch_forward<64, false, true>(p, grid, s) : launch_forward<64, false, false>(p, grid, s);
+    else e = c ? launch_forward<64, true, true>(p, grid, s) : launch_forward<64, true, false>(p, grid, s);
+  } else {
+    if (!bf16) e = c ? launch_forward<128, false, true>(p, grid, s) : launch_forward<128, false, false>(p, grid, s);
+    else e = c ? launch_forward<128, true, true>(p, grid, s) : launch_forward<128, true, false>(p, grid, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+}  // extern "C"

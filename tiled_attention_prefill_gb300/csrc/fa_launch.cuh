@@ -1,0 +1,35 @@
+// Kernel launcher template, explicitly instantiated in fa_inst_d64.cu / fa_inst_d128.cu so
+// that the eight kernel variants compile in parallel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "fa_kernel.cuh"
+
+namespace fa {
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_forward(const Params& p, int grid, cudaStream_t stream) {
+  using L = SmemLayout<D>;
+  auto kernel = fa_fwd_kernel<D, BF16, CAUSAL>;
+  // Opt in to the large dynamic shared-memory carve-out once per device.
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  kernel<<<grid, kNumThreads, L::kDynamicBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+#define FA_DECLARE_LAUNCH(EXT, D, BF16, CAUSAL) \
+  EXT template cudaError_t launch_forward<D, BF16, CAUSAL>(const Params&, int, cudaStream_t);
+
+}  // namespace fa

@@ -1,0 +1,133 @@
+"""Python binding of the C-ABI library ``libfa_gb300.so`` (ctypes).
+
+Argument marshalling only: every step of the attention forward pass runs in the
+library's CUDA kernel. PyTorch supplies device memory and the current stream.
+There is no fallback: if the library is missing or the device is unsupported,
+the call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
+
+FA_DTYPE_FP16 = 0
+FA_DTYPE_BF16 = 1
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_ALIGN = -3
+FA_ERR_CUDA = -4
+FA_ERR_TIMEOUT = -5
+FA_ERR_TOO_LARGE = -6
+
+# Every symbol include/fa.h declares, with its ctypes signature.
+SIGNATURES = {
+    "fa_forward": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                  ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "fa_error_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "fa_version": (ctypes.c_int, []),
+    "fa_check_device_status": (ctypes.c_int, []),
+    "fa_set_watchdog_ns": (ctypes.c_int, [ctypes.c_ulonglong]),
+    "fa_last_cuda_error": (ctypes.c_int, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__("fa error %d: %s" % (code, msg))
+        self.code = code
+
+
+def load_library(path: str | None = None):
+    """Load (once) and return the ctypes handle of the library; raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError("%s not built: run `python -c 'import __graft_entry__ as g; g.build()'` "
+                              "(needs nvcc for sm_103a)" % p)
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def error_string(code: int) -> str:
+    return load_library().fa_error_string(int(code)).decode()
+
+
+def _check(code: int):
+    if code != FA_OK:
+        msg = error_string(code)
+        if code == FA_ERR_CUDA:
+            msg += " (cudaError %d)" % load_library().fa_last_cuda_error()
+        raise FAError(code, msg)
+
+
+def check_device_status() -> None:
+    """Synchronise the current device and raise FAError if a kernel timed out."""
+    _check(load_library().fa_check_device_status())
+
+
+def set_watchdog_ns(ns: int) -> None:
+    _check(load_library().fa_set_watchdog_ns(int(ns)))
+
+
+def forward_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int, N: int, D: int,
+                scale: float, causal: bool, dtype: int, stream: int) -> int:
+    """Direct call of ``fa_forward`` with integer device pointers; returns the status code."""
+    return load_library().fa_forward(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr or None, int(B), int(H), int(N), int(D),
+                                     float(scale), int(bool(causal)), int(dtype), stream or None)
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, return_lse: bool = True):
+    """Attention forward on CUDA tensors [B, H, N, D] (fp16 or bf16, contiguous).
+
+    Returns (o, lse) with o like q and lse [B, H, N] fp32 (lse is None when
+    ``return_lse`` is False and no buffer was given). Runs on the current stream.
+    """
+    import torch
+
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share dtype fp16 or bf16")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, H, N, D]")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on the same device")
+    B, H, N, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device != q.device:
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous()
+                            or lse.device != q.device):
+        raise ValueError("lse must be a contiguous fp32 tensor [B, H, N]")
+    dtype = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
+    sc = -1.0 if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        rc = forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr() if lse is not None else 0, B, H, N, D, sc, causal, dtype, stream)
+    _check(rc)
+    return out, lse
