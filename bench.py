@@ -1,0 +1,377 @@
+"""Benchmark of the fused attention forward pass (one JSON line on stdout).
+
+A step is one forward pass (one kernel launch of the C-ABI library) over the
+headline workload: 1B-class LLM prefill attention, B=1, H=32, N=1024, D=64,
+fp16, causal, inputs resident in HBM. L2 is flushed (a 256 MiB write) before
+every timed step because the inputs (16 MiB) would otherwise stay in the 129 MB
+L2. Kernel time is taken with CUDA events on the launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
+                    [--workload c1..c5] [--kernel-only] [--no-sweep]
+
+--impl reference times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload per step). --kernel-only runs just the
+warm-up and timed kernel steps (the form used under ncu).
+
+Under torchrun each rank runs its own replica of the workload (the forward
+pass has no exchange step); value = all ranks' FLOPs / the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS and % of GB300 fp16/bf16 tensor peak; DRAM bytes vs min"
+UNIT = "TFLOP/s"
+HEADLINE = "c2"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["tiled_attention_prefill_gb300/csrc/" + f for f in
+                  ("fa_kernel.cuh", "ptx.cuh", "fa_launch.cuh", "fa_api.cu")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_dram_traffic.json")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def measured_traffic(workload: str):
+    """ncu DRAM bytes per launch for this workload, if taken on the current kernel sources."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    e = d.get("workloads", {}).get(workload)
+    if not e or e.get("kernel_sources_sha256_16") != kernel_source_hash():
+        return None
+    return e
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) while the GPU is busy; median SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", "fa_bench_clocks_%d_%d.csv" % (os.getpid(), index))
+
+    def start(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        busy = [r for r in rows if r[4].replace(".", "", 1).isdigit() and float(r[4]) > 0] or rows
+        sm = [float(r[1]) for r in busy if r[1].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(busy[0][2]) if busy[0][2].replace(".", "", 1).isdigit() else None,
+                "reasons": reasons, "samples": len(busy)}
+
+
+def dist_setup(want_gpu: bool):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if (want_gpu and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_desc(w):
+    return {"workload": "%s: %s" % (w.name, w.note), "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+            "dtype": w.dtype, "causal": w.causal, "scale": "1/sqrt(D)",
+            "values": "Q,K x%g N(0,1); V %s" % (w.qk_mult, "U(-1,1)" if w.v_uniform else "N(0,1)")}
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+def cpu_oracle_rate(w, budget_s: float = 12.0, max_heads=None):
+    """Time the oracle on whole heads of the workload until ~budget_s; returns (TFLOP/s, sample, threads)."""
+    import numpy as np
+
+    import oracle
+    from tiled_attention_prefill_gb300 import workloads
+
+    q, k, v = workloads.make_qkv(w)
+    q64, k64, v64 = (oracle.to_f64(x) for x in (q, k, v))
+    per_head = workloads.attention_flops(1, 1, w.N, w.D, w.causal)
+    threads = oracle.max_threads()
+    BH = w.B * w.H
+    done_heads, elapsed = 0, 0.0
+    h = 0
+    while (done_heads < max_heads) if max_heads is not None else (done_heads == 0 or elapsed < budget_s):
+        rows = np.stack([np.full(w.N, h % BH), np.arange(w.N)], axis=1)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q64, k64, v64, w.scale, w.causal, rows)
+        elapsed += time.perf_counter() - t0
+        done_heads += 1
+        h += 1
+    rate = per_head * done_heads / elapsed / 1e12
+    sample = "%d whole head(s) (all %d query rows each) of workload %s, fp64 oracle" % (done_heads, w.N, w.name)
+    return rate, sample, threads, elapsed
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup(want_gpu=False)
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    heads_per_step = 2
+    for _ in range(args.warmup):
+        cpu_oracle_rate(w, budget_s=0.0, max_heads=1)
+    rates, times = [], []
+    for _ in range(args.steps):
+        r, sample, threads, el = cpu_oracle_rate(w, budget_s=0.0, max_heads=heads_per_step)
+        rates.append(r)
+        times.append(el)
+    value = statistics.mean(rates)
+    flops_step = heads_per_step * (4.0 * w.N * w.N * w.D / (2 if w.causal else 1))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_desc(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "%d heads per step of workload %s (fp64 oracle, %.3g FLOP per step)"
+                                       % (heads_per_step, w.name, flops_step)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def time_kernel(fwd, steps, warmup, flush, stream):
+    """Per-step CUDA-event times (ms) of `fwd` on `stream`, L2 flushed before each step."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        fwd()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        fwd()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def run_fa(args, w):
+    import torch
+
+    world, rank, local = dist_setup(want_gpu=True)
+    from tiled_attention_prefill_gb300 import _build, fa, workloads
+
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_kind = load_peaks()
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    def measure(wl, steps, warmup):
+        q, k, v = (x.to(dev) for x in workloads.make_qkv(wl))
+        o = torch.empty_like(q)
+        lse = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device=dev)
+
+        def fwd():
+            fa.forward(q, k, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse)
+
+        times = time_kernel(fwd, steps, warmup, flush, stream)
+        fa.check_device_status()
+        flops = workloads.attention_flops(wl.B, wl.H, wl.N, wl.D, wl.causal)
+        return times, flops
+
+    sampler = ClockSampler(local) if not args.kernel_only else None
+    if sampler:
+        sampler.start()
+    times, flops = measure(w, args.steps, args.warmup)
+    ms_local = statistics.mean(times)
+    ms = max_over_ranks(ms_local)
+    value = world * flops / (ms * 1e-3) / 1e12
+    if args.kernel_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": UNIT, "ms_per_step": ms,
+                              "config": workload_desc(w), "kernel_only": True}), flush=True)
+        return 0
+
+    # end to end through the public API: pinned host inputs -> device -> forward -> host
+    q_h, k_h, v_h = (x.pin_memory() for x in workloads.make_qkv(w))
+    q_d, k_d, v_d = (torch.empty_like(x, device=dev) for x in (q_h, k_h, v_h))
+    o_d = torch.empty_like(q_d)
+    l_d = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    o_h = torch.empty_like(q_h).pin_memory()
+    l_h = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        fa.forward(q_d, k_d, v_d, causal=w.causal, scale=w.scale, out=o_d, lse=l_d)
+        o_h.copy_(o_d, non_blocking=True)
+        l_h.copy_(l_d, non_blocking=True)
+
+    e2e_times = time_kernel(e2e_step, args.steps, args.warmup, flush, stream)
+    e2e_ms = max_over_ranks(statistics.mean(e2e_times))
+    h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h))
+    d2h = o_h.numel() * o_h.element_size() + l_h.numel() * l_h.element_size()
+
+    sweep = {}
+    if not args.no_sweep:
+        for name, wl in workloads.WORKLOADS.items():
+            st = 20 if wl.N <= 4096 else 10
+            t, f = measure(wl, st, 3)
+            m = statistics.median(t)
+            tf = f / (m * 1e-3) / 1e12
+            tr = measured_traffic(name)
+            sweep[name] = {"ms_median": m, "ms_p10": sorted(t)[len(t) // 10], "ms_p90": sorted(t)[(9 * len(t)) // 10],
+                           "tflops": tf, "frac_of_peak": tf / peak_tf,
+                           "dram_bytes": tr["dram_bytes"] if tr else None,
+                           "dram_vs_min": (tr["dram_bytes"] / workloads.min_dram_bytes(wl.B, wl.H, wl.N, wl.D, with_lse=False))
+                           if tr else None}
+    clocks = sampler.stop() if sampler else None
+
+    if rank != 0:
+        return 0
+    from tiled_attention_prefill_gb300 import workloads as W
+    achieved = flops / (ms_local * 1e-3) / 1e12
+    tr = measured_traffic(w.name)
+    min_bytes = W.min_dram_bytes(w.B, w.H, w.N, w.D, with_lse=False)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": dict(workload_desc(w), l2="flushed before every timed step (256 MiB write)",
+                       parallelism="replicas" if world > 1 else "single GPU"),
+        "pct_of_peak": 100.0 * achieved / peak_tf,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "peak_source": "%s bf16_tflops (burst; fp16 dense rate equal)" % peak_kind,
+                     "traffic": tr["dram_bytes"] if tr else None,
+                     "traffic_vs_min": (tr["dram_bytes"] / min_bytes) if tr else None,
+                     "min_bytes": min_bytes},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if sweep:
+        line["workloads"] = sweep
+    if not args.no_cpu and world >= 1:
+        rate, sample, threads, el = cpu_oracle_rate(w)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+                                "seconds": el}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["fa", "reference"], default="fa")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--kernel-only", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("warmup raised to 3 (timing rule)")
+        args.warmup = 3
+    from tiled_attention_prefill_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_fa(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

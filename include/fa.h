@@ -23,6 +23,12 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -64,30 +70,44 @@ enum fa_status {
  * for a failed launch and device-side timeouts, which fa_check_device_status() reports.
  * Thread-safe; one-time per-device setup runs on first use.
  */
-int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
                float scale, int causal, int dtype, void* stream);
 
 /* Static description of a return code. Never NULL. */
-const char* fa_error_string(int code);
+FA_API const char* fa_error_string(int code);
 
 /* Library version as major*10000 + minor*100 + patch. */
-int fa_version(void);
+FA_API int fa_version(void);
 
 /*
  * Synchronises the current device, then returns FA_OK, or FA_ERR_TIMEOUT if any kernel of
  * this library on the current device gave up on a bounded wait since the last call (the
  * flag is cleared). FA_ERR_CUDA if the synchronisation itself fails.
  */
-int fa_check_device_status(void);
+FA_API int fa_check_device_status(void);
 
 /*
  * Sets the device-side wait limit, in nanoseconds, for launches that follow (process-wide).
  * 0 restores the default (2 s). Returns FA_OK.
  */
-int fa_set_watchdog_ns(unsigned long long ns);
+FA_API int fa_set_watchdog_ns(unsigned long long ns);
+
+/*
+ * Work decomposition for launches that follow (process-wide):
+ *   FA_DECOMP_AUTO (0)      choose by problem size (default);
+ *   FA_DECOMP_TWO_TILES (1) each work item is 256 query rows, two 128-row query tiles that
+ *                           share every K/V tile (half the K/V traffic per query row);
+ *   FA_DECOMP_SPLIT_KV (2)  each work item is one 128-row query tile whose K/V tiles are split
+ *                           between the two softmax warpgroups and merged at the end (twice
+ *                           the items, half the serial chain: for short or few sequences).
+ * All three compute the same result (up to floating-point rounding order). Returns FA_OK or
+ * FA_ERR_INVALID_ARG for an unknown value.
+ */
+enum fa_decomposition { FA_DECOMP_AUTO = 0, FA_DECOMP_TWO_TILES = 1, FA_DECOMP_SPLIT_KV = 2 };
+FA_API int fa_set_decomposition(int mode);
 
 /* The cudaError_t value behind the most recent FA_ERR_CUDA returned on this host thread. */
-int fa_last_cuda_error(void);
+FA_API int fa_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

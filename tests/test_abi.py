@@ -108,3 +108,11 @@ def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(ImportError):
         fa.load_library(str(tmp_path / "libmissing.so"))
     assert isinstance(ctypes.CDLL, type)
+
+
+def test_decomposition_setter(lib):
+    assert lib.fa_set_decomposition(1) == fa.FA_OK
+    assert lib.fa_set_decomposition(2) == fa.FA_OK
+    assert lib.fa_set_decomposition(3) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_set_decomposition(-1) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_set_decomposition(0) == fa.FA_OK

@@ -47,16 +47,38 @@ SMALL_SHAPES = [
 ]
 
 
+DECOMPS = {"two_tiles": fa.FA_DECOMP_TWO_TILES, "split_kv": fa.FA_DECOMP_SPLIT_KV}
+
+
+@pytest.fixture
+def decomposition(request):
+    fa.set_decomposition(DECOMPS[request.param])
+    yield request.param
+    fa.set_decomposition(fa.FA_DECOMP_AUTO)
+
+
+@pytest.mark.parametrize("decomposition", list(DECOMPS), indirect=True)
 @pytest.mark.parametrize("shape", SMALL_SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-def test_small_shapes_against_oracle(shape, dtype, causal):
+def test_small_shapes_against_oracle(shape, dtype, causal, decomposition):
     B, H, N, D = shape
     w = workloads.Workload("t", B, H, N, D, dtype, causal, seed=7 * N + D + B)
     q, k, v = workloads.make_qkv(w)
     o, lse = run_cuda(q, k, v, causal, w.scale)
     ro, rl = oracle.attention(q, k, v, w.scale, causal)
-    assert_close(o, lse, ro, rl, dtype, str(shape))
+    assert_close(o, lse, ro, rl, dtype, "%s %s" % (shape, decomposition))
+
+
+@pytest.mark.parametrize("decomposition", list(DECOMPS), indirect=True)
+@pytest.mark.parametrize("name", ["c1", "c2", "c3c"])
+def test_workload_both_decompositions(name, decomposition):
+    """The same workloads forced through each decomposition."""
+    w = workloads.WORKLOADS[name]
+    q, k, v = workloads.make_qkv(w)
+    o, lse = run_cuda(q, k, v, w.causal, w.scale)
+    ro, rl = oracle.attention(q, k, v, w.scale, w.causal)
+    assert_close(o, lse, ro, rl, w.dtype, name + " " + decomposition)
 
 
 @pytest.mark.parametrize("name", ["c1", "c2", "c3", "c3c"])

@@ -22,7 +22,10 @@ LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 SOURCES = ["fa_api.cu", "fa_inst_d64.cu", "fa_inst_d128.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# Only the fa_* C entry points are exported (FA_API); everything else stays hidden so that two
+# copies of the library, or another library with the same C++ names, cannot interpose.
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
+          "-Xcompiler", "-fvisibility=hidden",
           "--expt-relaxed-constexpr"]
 
 

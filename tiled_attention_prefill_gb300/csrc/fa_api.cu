@@ -30,6 +30,7 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 constexpr long long kL2SectionBytes = 32ll << 20;  // K+V bytes of the heads kept close in time
 
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int> g_decomposition{FA_DECOMP_AUTO};
 thread_local int t_last_cuda_error = 0;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -131,6 +132,12 @@ int fa_set_watchdog_ns(unsigned long long ns) {
   return FA_OK;
 }
 
+int fa_set_decomposition(int mode) {
+  if (mode != FA_DECOMP_AUTO && mode != FA_DECOMP_TWO_TILES && mode != FA_DECOMP_SPLIT_KV) return FA_ERR_INVALID_ARG;
+  fa::g_decomposition.store(mode);
+  return FA_OK;
+}
+
 int fa_check_device_status(void) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -163,8 +170,8 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
 
   const long long BH = static_cast<long long>(B) * H;
-  const long long num_mb = (static_cast<long long>(N) + kItemRows - 1) / kItemRows;
-  if (N > (1 << 30) || BH > 0x7fffffffll || BH * num_mb > 0x7fffffffll) return FA_ERR_TOO_LARGE;
+  const long long num_qt = (static_cast<long long>(N) + kBM - 1) / kBM;  // 128-row query tiles
+  if (N > (1 << 30) || BH > 0x7fffffffll || BH * num_qt > 0x7fffffffll) return FA_ERR_TOO_LARGE;
   const size_t tensor_bytes = static_cast<size_t>(BH) * N * D * 2;
   const size_t lse_bytes = static_cast<size_t>(BH) * N * sizeof(float);
   if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
@@ -181,6 +188,27 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   const bool bf16 = dtype == FA_DTYPE_BF16;
   if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
 
+  // Work decomposition. Two query tiles per item halve the K/V traffic per query row; when
+  // that leaves too few items to fill the GPU (short or few sequences), each item is a single
+  // query tile whose K/V range is split between the two softmax warpgroups instead.
+  const long long items_two = BH * ((static_cast<long long>(N) + item_rows(false) - 1) / item_rows(false));
+  const int decomp = g_decomposition.load();
+  bool splitk = decomp == FA_DECOMP_SPLIT_KV;
+  if (decomp == FA_DECOMP_AUTO) {
+    if (causal) {
+      // Unequal item costs are balanced by dispatch order; split only when the GPU is not full.
+      splitk = items_two < info->num_sms;
+    } else {
+      // Equal item costs: compare how well each item count fills whole waves of SMs. The
+      // split-KV form pays a few percent for its extra K/V traffic and merge.
+      auto wave_eff = [&](long long n) {
+        const long long waves = (n + info->num_sms - 1) / info->num_sms;
+        return static_cast<double>(n) / static_cast<double>(waves * info->num_sms);
+      };
+      splitk = wave_eff(2 * items_two) * 0.96 > wave_eff(items_two);
+    }
+  }
+
   Params p{};
   if ((rc = encode_map(&p.tm_q, q, bf16, static_cast<int>(BH), N, D, kBM)) != FA_OK) return rc;
   if ((rc = encode_map(&p.tm_k, k, bf16, static_cast<int>(BH), N, D, kBN)) != FA_OK) return rc;
@@ -191,23 +219,30 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   p.timeout_ns = g_timeout_ns.load();
   p.BH = static_cast<int>(BH);
   p.N = N;
-  p.num_mb = static_cast<int>(num_mb);
-  p.num_items = static_cast<int>(BH * num_mb);
+  p.num_mb = static_cast<int>((static_cast<long long>(N) + item_rows(splitk) - 1) / item_rows(splitk));
+  p.num_items = static_cast<int>(BH * p.num_mb);
   const long long kv_head_bytes = 2ll * N * D * 2;
   long long section = kL2SectionBytes / (kv_head_bytes > 0 ? kv_head_bytes : 1);
   p.section = static_cast<int>(section < 1 ? 1 : (section > BH ? BH : section));
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
-  const int grid = p.num_items < info->num_sms ? p.num_items : info->num_sms;
+  // Grid. Persistent (one CTA per SM, items strided in snake order) unless the items have
+  // very unequal cost (causal) and there are several waves of them: then one CTA per item,
+  // dispatched by the hardware in longest-first order, balances better.
+  const bool per_item = causal != 0 && p.num_items > 2 * info->num_sms;
+  const int grid = (per_item || p.num_items < info->num_sms) ? p.num_items : info->num_sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool c = causal != 0;
+#define FA_LAUNCH(DD, BB, CC)                                                                    \
+  (splitk ? launch_forward<DD, BB, CC, true>(p, grid, s) : launch_forward<DD, BB, CC, false>(p, grid, s))
   if (D == 64) {
-    if (!bf16) e = c ? launch_forward<64, false, true>(p, grid, s) : launch_forward<64, false, false>(p, grid, s);
-    else e = c ? launch_forward<64, true, true>(p, grid, s) : launch_forward<64, true, false>(p, grid, s);
+    if (!bf16) e = c ? FA_LAUNCH(64, false, true) : FA_LAUNCH(64, false, false);
+    else e = c ? FA_LAUNCH(64, true, true) : FA_LAUNCH(64, true, false);
   } else {
-    if (!bf16) e = c ? launch_forward<128, false, true>(p, grid, s) : launch_forward<128, false, false>(p, grid, s);
-    else e = c ? launch_forward<128, true, true>(p, grid, s) : launch_forward<128, true, false>(p, grid, s);
+    if (!bf16) e = c ? FA_LAUNCH(128, false, true) : FA_LAUNCH(128, false, false);
+    else e = c ? FA_LAUNCH(128, true, true) : FA_LAUNCH(128, true, false);
   }
+#undef FA_LAUNCH
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
 }

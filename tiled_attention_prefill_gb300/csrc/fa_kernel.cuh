@@ -11,22 +11,27 @@
 // denominator l, rescales the accumulated O by exp(m_old - m_new) when the max grows, and
 // normalises once at the end. The mapping onto GB300 is this file's own:
 //
-//   * One CTA per SM (persistent), 320 threads = 10 warps:
-//       warps 0-3  softmax warpgroup for query tile 0 of the work item (one thread per row)
-//       warps 4-7  softmax warpgroup for query tile 1
-//       warp  8    tcgen05 MMA issuer (one thread) and TMEM owner
+//   * One CTA per SM, 320 threads = 10 warps:
+//       warps 0-3  softmax warpgroup 0 (one thread per query row, TMEM lane = row)
+//       warps 4-7  softmax warpgroup 1
+//       warp  8    tcgen05 MMA issuer (warp-uniform, one elected lane issues) and TMEM owner
 //       warp  9    TMA producer (one thread)
-//   * A work item is (batch*head, 256 query rows) = two 128-row query tiles sharing every
-//     K/V tile that is loaded. K and V tiles (128 keys x D) stream through a shared-memory
-//     ring filled by TMA (128-byte swizzle), synchronised with mbarriers.
-//   * S = Q K^T for each query tile goes to its own 128 TMEM columns (fp32). The softmax
-//     warpgroup reads its row of S (tcgen05.ld, lane = row), writes P as fp16/bf16 back into
-//     the same TMEM columns, and the MMA warp computes O += P V with P read from TMEM.
-//     O (fp32, D columns per query tile) stays in TMEM for the whole K/V loop.
-//   * The max used in the exponent is only moved when a tile raises the row max by more than
+//   * K and V tiles (128 keys x D) stream through a shared-memory ring filled by TMA
+//     (128-byte swizzle) in exactly the order the MMA warp consumes them.
+//   * S = Q K^T for a warpgroup goes to its own 128 TMEM columns (fp32). The warpgroup reads
+//     its row of S (tcgen05.ld), writes P as fp16/bf16 back into the same columns, and the MMA
+//     warp computes O += P V with P read from TMEM. O (fp32, D columns per warpgroup) stays in
+//     TMEM for the whole K/V loop.
+//   * Two work decompositions (template SPLITK):
+//       false: a work item is 256 query rows = two 128-row query tiles, one per warpgroup,
+//              sharing every K/V tile loaded (half the K/V traffic per query row).
+//       true:  a work item is one 128-row query tile; warpgroup 0 takes the even K/V tiles,
+//              warpgroup 1 the odd ones, and warpgroup 0 merges the two partial (m, l, O) at
+//              the end with the same rescaling rule. Twice the work items and half the serial
+//              chain per item: used when there are too few items to fill the GPU.
+//   * The max used in the exponent only moves when a tile raises the row max by more than
 //     2^8; otherwise p = 2^(x - m_used) may exceed 1 (at most 256). O and l always carry the
-//     same factor, so the final O / l is unchanged; the rescale of O in TMEM is skipped in
-//     most iterations.
+//     same factor, so O / l is unchanged, and the O rescale in TMEM is rarely needed.
 //   * Causal: K/V tiles to the right of a query tile's diagonal are never loaded or
 //     multiplied; only the diagonal tile applies an element mask.
 //   * Epilogue: O / l -> fp16/bf16 -> swizzled shared memory -> TMA store; lse in fp32.
@@ -46,14 +51,14 @@ namespace fa {
 
 constexpr int kBM = 128;        // query rows per query tile (tcgen05 M)
 constexpr int kBN = 128;        // keys per K/V tile (tcgen05 N of S = QK^T)
-constexpr int kQTiles = 2;      // query tiles per work item
-constexpr int kItemRows = kBM * kQTiles;
 constexpr int kNumThreads = 320;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kTmemCols = 512;  // S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.693147180559945309f;
+
+__host__ __device__ constexpr int item_rows(bool splitk) { return splitk ? kBM : 2 * kBM; }
 
 // Status bits written by the kernel (host reads them through fa_check_device_status).
 constexpr unsigned kStatusTimeout = 1u;
@@ -68,7 +73,7 @@ struct Params {
   unsigned long long timeout_ns;
   int BH;
   int N;
-  int num_mb;                  // ceil(N / 256)
+  int num_mb;                  // row blocks per head: ceil(N / item_rows)
   int num_items;               // BH * num_mb
   int section;                 // causal ordering: heads per L2 section
   float scale_log2;            // scale * log2(e)
@@ -81,18 +86,20 @@ struct SmemLayout {
   static constexpr int kTileBytes = kBM * D * 2;   // a 128 x D fp16/bf16 tile
   static constexpr int kStages = (D == 64) ? 6 : 3;
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
-  static constexpr int kOOff = kKVOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kOOff + kQTiles * kTileBytes;
+  static constexpr int kKVOff = kQOff + 2 * kTileBytes;
+  static constexpr int kOOff = kKVOff + kStages * kTileBytes;  // two staging tiles for O
+  static constexpr int kBarOff = kOOff + 2 * kTileBytes;
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kQEmpty = 1;
   static constexpr int kKVFull = 2;
   static constexpr int kKVEmpty = kKVFull + kStages;
-  static constexpr int kSFull = kKVEmpty + kStages;  // [2]
-  static constexpr int kPFull = kSFull + 2;          // [2]
-  static constexpr int kOFull = kPFull + 2;          // [2]
-  static constexpr int kDrain = kOFull + 2;
+  static constexpr int kSFull = kKVEmpty + kStages;  // [2] S of warpgroup i is in TMEM
+  static constexpr int kPFull = kSFull + 2;          // [2] P of warpgroup i is in TMEM
+  static constexpr int kOFull = kPFull + 2;          // [2] last PV of warpgroup i completed
+  static constexpr int kStats = kOFull + 2;          // split-K: warpgroup 1 published (m, l)
+  static constexpr int kO1Free = kStats + 1;         // split-K: warpgroup 0 finished reading O1
+  static constexpr int kDrain = kO1Free + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
@@ -136,7 +143,7 @@ __device__ __forceinline__ bool wait_phase_drain(uint32_t bar, uint32_t parity) 
 
 struct Item {
   int bh;
-  int mb;
+  int mb;  // row block: 256 rows (two query tiles) or, split-K, one 128-row query tile
 };
 
 // Work-item order. Non-causal: head-major (all row blocks of a head run close together, so
@@ -159,21 +166,29 @@ __device__ __forceinline__ Item decode_item(int t, const Params& p) {
   return it;
 }
 
-// Number of K/V tiles each query tile of row block mb visits (0 = tile lies beyond N).
-template <bool CAUSAL>
-__device__ __forceinline__ void tile_counts(int mb, int N, int& n0, int& n1) {
+// Per work item: nk = K/V tiles loaded, n[w] = K/V tiles processed by warpgroup w (0 = idle).
+template <bool CAUSAL, bool SPLITK>
+__device__ __forceinline__ void tile_counts(int mb, int N, int& nk, int& n0, int& n1) {
   const int nkt = (N + kBN - 1) / kBN;
-  const bool t1 = mb * kItemRows + kBM < N;
-  if (CAUSAL) {
-    n0 = min(2 * mb + 1, nkt);
-    n1 = t1 ? min(2 * mb + 2, nkt) : 0;
+  if (SPLITK) {
+    nk = CAUSAL ? min(mb + 1, nkt) : nkt;
+    n0 = (nk + 1) >> 1;
+    n1 = nk >> 1;
   } else {
-    n0 = nkt;
-    n1 = t1 ? nkt : 0;
+    const bool t1 = mb * 2 * kBM + kBM < N;
+    if (CAUSAL) {
+      n0 = min(2 * mb + 1, nkt);
+      n1 = t1 ? min(2 * mb + 2, nkt) : 0;
+    } else {
+      n0 = nkt;
+      n1 = t1 ? nkt : 0;
+    }
+    nk = max(n0, n1);
   }
 }
 
-// k-th work item of this CTA in snake order over the sorted item list (-1 when done).
+// k-th work item of this CTA in snake order over the sorted item list (-1 when done). With
+// one CTA per item (gridDim.x == num_items) this is just blockIdx.x.
 __device__ __forceinline__ int item_of(int k, int num_items) {
   const int G = gridDim.x;
   const long long base = static_cast<long long>(k) * G;
@@ -183,9 +198,10 @@ __device__ __forceinline__ int item_of(int k, int num_items) {
   return t < num_items ? static_cast<int>(t) : -1;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPLITK>
 __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   using L = SmemLayout<D>;
+  constexpr int kItemRows = item_rows(SPLITK);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
@@ -196,6 +212,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
   auto q_addr = [&](int i) -> uint32_t { return sbase + L::kQOff + i * L::kTileBytes; };
   auto kv_addr = [&](int s) -> uint32_t { return sbase + L::kKVOff + s * L::kTileBytes; };
   auto o_addr = [&](int i) -> uint32_t { return sbase + L::kOOff + i * L::kTileBytes; };
+  // split-K: warpgroup 1 never stages O, so its staging tile carries the (m, l) hand-off
+  float* stats_m = reinterpret_cast<float*>(smem + L::kOOff + L::kTileBytes);
+  float* stats_l = stats_m + kBM;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   const Watch watch{abort_flag, p.status, p.timeout_ns};
@@ -212,6 +231,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
       mbar_init(bar(L::kPFull + i), kBM);
       mbar_init(bar(L::kOFull + i), 1);
     }
+    mbar_init(bar(L::kStats), kBM);
+    mbar_init(bar(L::kO1Free), kBM);
     mbar_init(bar(L::kDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -236,32 +257,39 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
     if (lane == 0) {
       uint32_t kv_pos = 0, q_loads = 0;
       bool ok = true;
+      auto load_kv = [&](const void* tm, int j, int bh) -> bool {
+        const uint32_t s = kv_pos % L::kStages;
+        if (!wait_phase(bar(L::kKVEmpty + s), ((kv_pos / L::kStages) & 1) ^ 1, watch, 1)) return false;
+        mbar_arrive_expect_tx(bar(L::kKVFull + s), L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(kv_addr(s) + c * L::kChunkBytes, tm, bar(L::kKVFull + s), c * 64, j * kBN, bh);
+        ++kv_pos;
+        return true;
+      };
       for (int k = 0; ok; ++k) {
         const int t = item_of(k, p.num_items);
         if (t < 0) break;
         const Item it = decode_item<CAUSAL>(t, p);
-        int n0, n1;
-        tile_counts<CAUSAL>(it.mb, p.N, n0, n1);
-        const int nk = max(n0, n1);
+        int nk, n0, n1;
+        tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
         // Q tiles: wait until every S MMA of the previous item has read them.
         if (!(ok = wait_phase(bar(L::kQEmpty), (q_loads & 1) ^ 1, watch, 0))) break;
-        const int nq = n1 > 0 ? 2 : 1;
+        const int nq = (!SPLITK && n1 > 0) ? 2 : 1;
         mbar_arrive_expect_tx(bar(L::kQFull), nq * L::kTileBytes);
         for (int i = 0; i < nq; ++i)
           for (int c = 0; c < L::kChunks; ++c)
             tma_load_3d(q_addr(i) + c * L::kChunkBytes, &p.tm_q, bar(L::kQFull), c * 64,
                         it.mb * kItemRows + i * kBM, it.bh);
         ++q_loads;
-        for (int j = 0; j < nk && ok; ++j) {
-          for (int kv = 0; kv < 2; ++kv) {
-            const uint32_t s = kv_pos % L::kStages;
-            const uint32_t ph = (kv_pos / L::kStages) & 1;
-            if (!(ok = wait_phase(bar(L::kKVEmpty + s), ph ^ 1, watch, 1))) break;
-            mbar_arrive_expect_tx(bar(L::kKVFull + s), L::kTileBytes);
-            const void* tm = kv == 0 ? static_cast<const void*>(&p.tm_k) : static_cast<const void*>(&p.tm_v);
-            for (int c = 0; c < L::kChunks; ++c)
-              tma_load_3d(kv_addr(s) + c * L::kChunkBytes, tm, bar(L::kKVFull + s), c * 64, j * kBN, it.bh);
-            ++kv_pos;
+        // K/V in the MMA warp's consumption order:
+        //   two query tiles: K0 V0 K1 V1 ...      split-K: K0 K1 V0 K2 V1 K3 V2 ...
+        if (!SPLITK) {
+          for (int j = 0; j < nk && ok; ++j) ok = load_kv(&p.tm_k, j, it.bh) && load_kv(&p.tm_v, j, it.bh);
+        } else {
+          ok = load_kv(&p.tm_k, 0, it.bh);
+          for (int j = 0; j < nk && ok; ++j) {
+            if (j + 1 < nk) ok = load_kv(&p.tm_k, j + 1, it.bh);
+            ok = ok && load_kv(&p.tm_v, j, it.bh);
           }
         }
       }
@@ -278,122 +306,161 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop; one elected lane issues each tcgen05 instruction.
+    {
+      const uint32_t leader = elect_one_lane();
       constexpr uint32_t idesc_s = instr_desc_f16(BF16, kBM, kBN, false);
       constexpr uint32_t idesc_o = instr_desc_f16(BF16, kBM, D, true);
-      uint32_t kv_pos = 0, items = 0;
-      uint32_t pcnt[2] = {0, 0};
+      uint32_t kv_pos = 0, items = 0, merges = 0;
+      uint32_t pcnt0 = 0, pcnt1 = 0;  // P hand-offs consumed per warpgroup
       bool ok = true;
+      auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
+        return __all_sync(0xffffffffu, wait_phase(b, parity, watch, site));
+      };
+      // Next K/V ring slot: wait until TMA has filled it; returns its stage.
+      auto next_slot = [&](uint32_t& stage) -> bool {
+        stage = kv_pos % L::kStages;
+        if (!wait(bar(L::kKVFull + stage), (kv_pos / L::kStages) & 1, 3)) return false;
+        ++kv_pos;
+        tc_fence_after();
+        return true;
+      };
 
-      // S_i = Q_i K^T into TMEM columns [128 i, 128 i + 128).
-      auto issue_s = [&](int i, uint32_t stage) {
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(i * kBN);
+      // Descriptors are built once; per stage / tile / k-step only the 14-bit start-address
+      // field (address >> 4, no carry possible below 256 KB) is advanced.
+      const uint64_t q_desc = smem_desc_sw128(q_addr(0), 16, 1024);
+      const uint64_t k_desc = smem_desc_sw128(kv_addr(0), 16, 1024);
+      const uint64_t v_desc = smem_desc_sw128(kv_addr(0), L::kChunkBytes, 1024);
+      constexpr uint32_t kTileEnc = L::kTileBytes >> 4;
+
+      // S_w = Q_qi K^T into TMEM columns [128 w, 128 w + 128).
+      auto issue_s = [&](int w, int qi, uint32_t stage) {
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(w * kBN);
+        const uint64_t a0 = q_desc + static_cast<uint32_t>(qi) * kTileEnc;
+        const uint64_t b0 = k_desc + stage * kTileEnc;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          const uint64_t a = smem_desc_sw128(q_addr(i) + off, 16, 1024);
-          const uint64_t b = smem_desc_sw128(kv_addr(stage) + off, 16, 1024);
-          mma_ss(d_tmem, a, b, idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss_leader(d_tmem, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u, leader);
         }
+        mma_commit_leader(bar(L::kSFull + w), leader);
       };
-      // O_i (+)= P_i V; P_i (fp16/bf16, 64 columns) sits in the first half of S_i's columns.
-      auto issue_pv = [&](int i, uint32_t stage, bool accumulate) {
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(2 * kBN + i * D);
-        const uint32_t a_tmem = tmem + static_cast<uint32_t>(i * kBN);
+      // O_w (+)= P_w V; P_w (fp16/bf16, 64 columns) sits in the first half of S_w's columns.
+      // V tile: keys are the K dimension (rows, 128 B apart), D is the N dimension (MN-major):
+      // 8-key groups are 1024 B apart, 64-column chunks kChunkBytes apart (the LBO).
+      auto issue_pv = [&](int w, uint32_t stage, bool accumulate, bool last) -> bool {
+        const uint32_t pc = w ? pcnt1 : pcnt0;
+        if (!wait(bar(L::kPFull + w), pc & 1, 5 + w)) return false;
+        if (w) ++pcnt1;
+        else ++pcnt0;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(2 * kBN + w * D);
+        const uint32_t a_tmem = tmem + static_cast<uint32_t>(w * kBN);
+        const uint64_t b0 = v_desc + stage * kTileEnc;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // V tile: keys are the K dimension (rows, 128 B apart), D is the N dimension
-          // (MN-major): 8-key groups are 1024 B apart, 64-column chunks kChunkBytes apart.
-          const uint64_t b = smem_desc_sw128(kv_addr(stage) + kk * 16 * 128, L::kChunkBytes, 1024);
-          mma_ts(d_tmem, a_tmem + kk * 8, b, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts_leader(d_tmem, a_tmem + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_o,
+                        (accumulate || kk > 0) ? 1u : 0u, leader);
+        if (last) mma_commit_leader(bar(L::kOFull + w), leader);
+        return true;
       };
+      auto release = [&](uint32_t stage) { mma_commit_leader(bar(L::kKVEmpty + stage), leader); };
 
       for (int k = 0; ok; ++k) {
         const int t = item_of(k, p.num_items);
         if (t < 0) break;
         const Item it = decode_item<CAUSAL>(t, p);
-        int n[2];
-        tile_counts<CAUSAL>(it.mb, p.N, n[0], n[1]);
-        const int nk = max(n[0], n[1]);
-        if (!(ok = wait_phase(bar(L::kQFull), items & 1, watch, 2))) break;
-        // prologue: S_i for K tile 0
-        uint32_t sk = kv_pos % L::kStages;
-        if (!(ok = wait_phase(bar(L::kKVFull + sk), (kv_pos / L::kStages) & 1, watch, 3))) break;
-        ++kv_pos;
-        tc_fence_after();
-        for (int i = 0; i < 2; ++i)
-          if (n[i] > 0) {
-            issue_s(i, sk);
-            mma_commit(bar(L::kSFull + i));
-          }
-        mma_commit(bar(L::kKVEmpty + sk));
-        for (int j = 0; j < nk && ok; ++j) {
-          const uint32_t sv = kv_pos % L::kStages;
-          if (!(ok = wait_phase(bar(L::kKVFull + sv), (kv_pos / L::kStages) & 1, watch, 4))) break;
-          ++kv_pos;
-          tc_fence_after();
-          bool k_next = false;
-          uint32_t sk2 = 0;
-          for (int i = 0; i < 2 && ok; ++i) {
-            if (j < n[i]) {
-              if (!(ok = wait_phase(bar(L::kPFull + i), pcnt[i] & 1, watch, 5 + i))) break;
-              ++pcnt[i];
-              tc_fence_after();
-              issue_pv(i, sv, j > 0);
-              if (j == n[i] - 1) mma_commit(bar(L::kOFull + i));
-            }
-            if (j + 1 < n[i]) {
-              if (!k_next) {
-                sk2 = kv_pos % L::kStages;
-                if (!(ok = wait_phase(bar(L::kKVFull + sk2), (kv_pos / L::kStages) & 1, watch, 7))) break;
-                ++kv_pos;
-                tc_fence_after();
+        int nk, n0, n1;
+        tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
+        if (!(ok = wait(bar(L::kQFull), items & 1, 2))) break;
+        uint32_t sk, sv;
+        if (!SPLITK) {
+          // Both query tiles against K0, then per K/V tile j: PV_w(j) and S_w(j+1), w = 0, 1.
+          if (!(ok = next_slot(sk))) break;
+          issue_s(0, 0, sk);
+          if (n1 > 0) issue_s(1, 1, sk);
+          release(sk);
+          for (int j = 0; j < nk && ok; ++j) {
+            if (!(ok = next_slot(sv))) break;
+            bool k_next = false;
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              const int nw = w ? n1 : n0;
+              if (j < nw && !(ok = issue_pv(w, sv, j > 0, j == nw - 1))) break;
+              if (j + 1 < nw) {
+                if (!k_next && !(ok = next_slot(sk))) break;
                 k_next = true;
+                issue_s(w, w, sk);
               }
-              issue_s(i, sk2);
-              mma_commit(bar(L::kSFull + i));
+            }
+            if (!ok) break;
+            release(sv);
+            if (k_next) release(sk);
+          }
+        } else {
+          // One query tile; K/V tile j belongs to warpgroup j & 1.
+          //   S_0(K0), S_1(K1), then per j: PV_{j&1}(V_j), S_{j&1}(K_{j+2}).
+          if (!(ok = next_slot(sk))) break;
+          issue_s(0, 0, sk);
+          release(sk);
+          if (nk > 1) {
+            if (!(ok = next_slot(sk))) break;
+            issue_s(1, 0, sk);
+            release(sk);
+          }
+          for (int j = 0; j < nk && ok; ++j) {
+            const int w = j & 1;
+            if (!(ok = next_slot(sv))) break;
+            // O1 is overwritten by the first PV of warpgroup 1: the previous item's merge
+            // must have read it.
+            if (j == 1 && merges > 0 && !(ok = wait(bar(L::kO1Free), (merges - 1) & 1, 13))) break;
+            if (!(ok = issue_pv(w, sv, j >= 2, j + 2 >= nk))) break;
+            release(sv);
+            if (j + 2 < nk) {
+              if (!(ok = next_slot(sk))) break;
+              issue_s(w, 0, sk);
+              release(sk);
             }
           }
-          if (!ok) break;
-          mma_commit(bar(L::kKVEmpty + sv));
-          if (k_next) mma_commit(bar(L::kKVEmpty + sk2));
+          if (ok && n1 > 0) ++merges;
         }
         if (!ok) break;
-        mma_commit(bar(L::kQEmpty));
+        mma_commit_leader(bar(L::kQEmpty), leader);
         ++items;
       }
       // Whatever happened, wait for every issued MMA before TMEM can be freed.
-      mma_commit(bar(L::kDrain));
-      wait_phase_drain(bar(L::kDrain), 0);
+      mma_commit_leader(bar(L::kDrain), leader);
+      if (leader) wait_phase_drain(bar(L::kDrain), 0);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    const int wg = warp >> 2;        // query tile of the item handled by this warpgroup
+    const int wg = warp >> 2;        // warpgroup: query tile (two-tile items) or K parity (split-K)
     const int wq = warp & 3;         // TMEM lane quarter accessible to this warp
     const int r = wq * 32 + lane;    // row within the query tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t t_s = tmem + lane_off + static_cast<uint32_t>(wg * kBN);
     const uint32_t t_o = tmem + lane_off + static_cast<uint32_t>(2 * kBN + wg * D);
+    const uint32_t t_o1 = tmem + lane_off + static_cast<uint32_t>(2 * kBN + D);
     const float sl2 = p.scale_log2;
-    uint32_t scnt = 0, ocnt = 0;
+    uint32_t scnt = 0, ocnt = 0, o1cnt = 0, mcnt = 0;
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
       const int t = item_of(k, p.num_items);
       if (t < 0) break;
       const Item it = decode_item<CAUSAL>(t, p);
-      int n0, n1;
-      tile_counts<CAUSAL>(it.mb, p.N, n0, n1);
+      int nk, n0, n1;
+      tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
       const int n_mine = wg == 0 ? n0 : n1;
       if (n_mine == 0) continue;
-      const int row = it.mb * kItemRows + wg * kBM + r;  // query index within the sequence
-      const int qt = 2 * it.mb + wg;                     // query tile index (diagonal K tile)
+      const int qt = SPLITK ? it.mb : 2 * it.mb + wg;  // query tile index (its diagonal K tile)
+      const int row = qt * kBM + r;                     // query index within the sequence
       float m_used = -INFINITY;
       float l_run = 0.f;
 
-      for (int j = 0; j < n_mine; ++j) {
+      for (int jj = 0; jj < n_mine; ++jj) {
+        const int j = SPLITK ? 2 * jj + wg : jj;  // K/V tile index
         bool w_ok = wait_phase(bar(L::kSFull + wg), scnt & 1, watch, 8 + wg);
         if (!__all_sync(0xffffffffu, w_ok)) {
           ok = false;
@@ -414,18 +481,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           for (int c = 0; c < kBN; ++c)
             if (c > lim) s[c] = -INFINITY;
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // Row max of the raw scores (scale > 0, so it commutes with the scaling).
+        float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
 #pragma unroll
         for (int c = 4; c < kBN; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+          mx0 = max3(mx0, s[c], s[c + 1]);
+          mx1 = max3(mx1, s[c + 2], s[c + 3]);
         }
-        const float x_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const float x_max = fmaxf(mx0, mx1) * sl2;
         float alpha = 1.f;
         bool rescale = false;
-        if (j == 0) {
+        if (jj == 0) {
           m_used = x_max;
         } else if (x_max > m_used + kRescaleLog2) {
           alpha = ex2_approx(m_used - x_max);
@@ -433,22 +499,31 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           l_run *= alpha;
           rescale = true;
         }
-        const float neg_m = -m_used;
-        float ls0 = 0.f, ls1 = 0.f;
+        // p = 2^(s * scale * log2 e - m_used), two lanes per packed FMA / add.
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t negm2 = f2_pack(-m_used, -m_used);
+        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
         uint32_t pk[kBN / 2];
 #pragma unroll
         for (int c = 0; c < kBN / 2; ++c) {
-          const float p0 = ex2_approx(fmaf(s[2 * c], sl2, neg_m));
-          const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, neg_m));
-          ls0 += p0;
-          ls1 += p1;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm2), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          if (c & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
+          else acc0 = f2_add(acc0, f2_pack(p0, p1));
           pk[c] = pack2<BF16>(p0, p1);
         }
-        l_run += ls0 + ls1;
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(acc0, a0, a1);
+          f2_unpack(acc1, b0, b1);
+          l_run += (a0 + a1) + (b0 + b1);
+        }
         tmem_st32x32b_x64(t_s, pk);
         if (__any_sync(0xffffffffu, rescale)) {
-          // O row *= alpha (alpha = 1 for rows that keep their max). The PV MMA of the
-          // previous tile has completed: S of this tile was issued after it.
+          // O row *= alpha (alpha = 1 for rows that keep their max). The previous PV of this
+          // warpgroup has completed: this tile's S was issued after it.
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
             uint32_t o[32];
@@ -464,43 +539,89 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
       }
       if (!ok) break;
 
+      if (SPLITK && wg == 1) {
+        // Hand (m, l) of the odd K/V tiles to warpgroup 0, which merges and stores. The
+        // previous hand-off must have been read first (warpgroup 0 signals kO1Free).
+        if (mcnt > 0) {
+          const bool f_ok = wait_phase(bar(L::kO1Free), (mcnt - 1) & 1, watch, 14);
+          if (!__all_sync(0xffffffffu, f_ok)) {
+            ok = false;
+            break;
+          }
+        }
+        ++mcnt;
+        stats_m[r] = m_used;
+        stats_l[r] = l_run;
+        mbar_arrive(bar(L::kStats));
+        continue;
+      }
+
       // ---------------- epilogue: O / l -> staging shared memory -> TMA store; lse
       // Each warp stages and stores its own 32 rows, so no barrier spans warps.
       bool e_ok = wait_phase(bar(L::kOFull + wg), ocnt & 1, watch, 10 + wg);
       ++ocnt;
+      const bool merge = SPLITK && n1 > 0;
+      float a_self = 1.f, a_other = 0.f;
+      if (merge) {
+        // Partial results of the odd tiles: O1 in TMEM, (m1, l1) from warpgroup 1.
+        e_ok = e_ok && wait_phase(bar(L::kOFull + 1), o1cnt & 1, watch, 11);
+        e_ok = e_ok && wait_phase(bar(L::kStats), mcnt & 1, watch, 12);
+        ++o1cnt;
+        ++mcnt;
+      }
       if (!__all_sync(0xffffffffu, e_ok)) {
         ok = false;
         break;
+      }
+      if (merge) {
+        const float m1 = stats_m[r], l1 = stats_l[r];
+        const float m = fmaxf(m_used, m1);
+        a_self = ex2_approx(m_used - m);
+        a_other = ex2_approx(m1 - m);
+        l_run = l_run * a_self + l1 * a_other;
+        m_used = m;
       }
       if (lane == 0) bulk_wait_group_read0();  // this warp's previous store has left the buffer
       __syncwarp();
       tc_fence_after();
       const float inv_l = 1.0f / l_run;
+      const float c_self = a_self * inv_l, c_other = a_other * inv_l;
       const uint32_t ob = o_addr(wg);
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
         tmem_ld32x32b_x32(t_o + c, o);
+        if (merge) {
+          uint32_t o1[32];
+          tmem_ld32x32b_x32(t_o1 + c, o1);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            o[e] = __float_as_uint(__uint_as_float(o[e]) * c_self + __uint_as_float(o1[e]) * c_other);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c_self);
+        }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int col = c + 8 * u;         // first of the 8 columns in this 16-byte unit
           const int chunk = col >> 6;        // 64-column swizzle chunk
           const int unit = (col & 63) >> 3;  // 16-byte unit within the 128-byte row
           const uint32_t addr = ob + chunk * L::kChunkBytes + r * 128 + ((unit ^ (r & 7)) << 4);
-          const uint32_t w0 = pack2<BF16>(__uint_as_float(o[8 * u + 0]) * inv_l, __uint_as_float(o[8 * u + 1]) * inv_l);
-          const uint32_t w1 = pack2<BF16>(__uint_as_float(o[8 * u + 2]) * inv_l, __uint_as_float(o[8 * u + 3]) * inv_l);
-          const uint32_t w2 = pack2<BF16>(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
-          const uint32_t w3 = pack2<BF16>(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
+          const uint32_t w0 = pack2<BF16>(__uint_as_float(o[8 * u + 0]), __uint_as_float(o[8 * u + 1]));
+          const uint32_t w1 = pack2<BF16>(__uint_as_float(o[8 * u + 2]), __uint_as_float(o[8 * u + 3]));
+          const uint32_t w2 = pack2<BF16>(__uint_as_float(o[8 * u + 4]), __uint_as_float(o[8 * u + 5]));
+          const uint32_t w3 = pack2<BF16>(__uint_as_float(o[8 * u + 6]), __uint_as_float(o[8 * u + 7]));
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
                        : "memory");
         }
       }
+      tc_fence_before();
+      if (merge) mbar_arrive(bar(L::kO1Free));  // O1 and (m1, l1) consumed
       if (p.lse != nullptr && row < p.N)
         p.lse[static_cast<long long>(it.bh) * p.N + row] = (m_used + log2f(l_run)) * kLn2;
-      tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
-      const int row0_warp = it.mb * kItemRows + wg * kBM + wq * 32;
+      const int row0_warp = qt * kBM + wq * 32;
       if (lane == 0 && row0_warp < p.N) {  // rows past N are clipped by the store; skip empty boxes
         for (int c = 0; c < L::kChunks; ++c)
           tma_store_3d(&p.tm_o, ob + c * L::kChunkBytes + wq * 32 * 128, c * 64, row0_warp, it.bh);

@@ -10,10 +10,10 @@
 
 namespace fa {
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPLITK>
 cudaError_t launch_forward(const Params& p, int grid, cudaStream_t stream) {
   using L = SmemLayout<D>;
-  auto kernel = fa_fwd_kernel<D, BF16, CAUSAL>;
+  auto kernel = fa_fwd_kernel<D, BF16, CAUSAL, SPLITK>;
   // Opt in to the large dynamic shared-memory carve-out once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -29,7 +29,8 @@ cudaError_t launch_forward(const Params& p, int grid, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-#define FA_DECLARE_LAUNCH(EXT, D, BF16, CAUSAL) \
-  EXT template cudaError_t launch_forward<D, BF16, CAUSAL>(const Params&, int, cudaStream_t);
+#define FA_DECLARE_LAUNCH(EXT, D, BF16, CAUSAL)                                                       \
+  EXT template cudaError_t launch_forward<D, BF16, CAUSAL, false>(const Params&, int, cudaStream_t); \
+  EXT template cudaError_t launch_forward<D, BF16, CAUSAL, true>(const Params&, int, cudaStream_t);
 
 }  // namespace fa

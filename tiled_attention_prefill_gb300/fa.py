@@ -24,6 +24,9 @@ FA_ERR_ALIGN = -3
 FA_ERR_CUDA = -4
 FA_ERR_TIMEOUT = -5
 FA_ERR_TOO_LARGE = -6
+FA_DECOMP_AUTO = 0
+FA_DECOMP_TWO_TILES = 1
+FA_DECOMP_SPLIT_KV = 2
 
 # Every symbol include/fa.h declares, with its ctypes signature.
 SIGNATURES = {
@@ -35,6 +38,7 @@ SIGNATURES = {
     "fa_check_device_status": (ctypes.c_int, []),
     "fa_set_watchdog_ns": (ctypes.c_int, [ctypes.c_ulonglong]),
     "fa_last_cuda_error": (ctypes.c_int, []),
+    "fa_set_decomposition": (ctypes.c_int, [ctypes.c_int]),
 }
 
 _lock = threading.Lock()
@@ -86,6 +90,11 @@ def check_device_status() -> None:
 
 def set_watchdog_ns(ns: int) -> None:
     _check(load_library().fa_set_watchdog_ns(int(ns)))
+
+
+def set_decomposition(mode: int) -> None:
+    """Process-wide work decomposition (FA_DECOMP_AUTO / _TWO_TILES / _SPLIT_KV)."""
+    _check(load_library().fa_set_decomposition(int(mode)))
 
 
 def forward_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int, N: int, D: int,
