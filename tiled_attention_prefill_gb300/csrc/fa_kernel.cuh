@@ -11,11 +11,14 @@
 // denominator l, rescales the accumulated O by exp(m_old - m_new) when the max grows, and
 // normalises once at the end. The mapping onto GB300 is this file's own:
 //
-//   * One CTA per SM, 320 threads = 10 warps:
-//       warps 0-3  softmax warpgroup 0 (one thread per query row, TMEM lane = row)
-//       warps 4-7  softmax warpgroup 1
-//       warp  8    tcgen05 MMA issuer (warp-uniform, one elected lane issues) and TMEM owner
-//       warp  9    TMA producer (one thread)
+//   * One CTA per SM, 384 threads = 3 warpgroups:
+//       warps 0-3   softmax warpgroup 0 (one thread per query row, TMEM lane = row)
+//       warps 4-7   softmax warpgroup 1
+//       warp  8     tcgen05 MMA issuer (warp-uniform, one elected lane issues) and TMEM owner
+//       warp  9     TMA producer (one thread)
+//       warps 10-11 idle
+//     setmaxnreg moves registers from the third warpgroup (72 each) to the softmax
+//     warpgroups (216 each); 72 + 2 * 216 = 3 * 168, the launch allocation.
 //   * K and V tiles (128 keys x D) stream through a shared-memory ring filled by TMA
 //     (128-byte swizzle) in exactly the order the MMA warp consumes them.
 //   * S = Q K^T for a warpgroup goes to its own 128 TMEM columns (fp32). The warpgroup reads
@@ -51,11 +54,19 @@ namespace fa {
 
 constexpr int kBM = 128;        // query rows per query tile (tcgen05 M)
 constexpr int kBN = 128;        // keys per K/V tile (tcgen05 N of S = QK^T)
-constexpr int kNumThreads = 320;
+constexpr int kNumThreads = 384;
+constexpr int kLaunchRegs = 168;   // registers per thread at launch (65536 / 384, rounded down to 8)
+constexpr int kSoftmaxRegs = 216;  // after setmaxnreg, softmax warpgroups
+constexpr int kOtherRegs = 72;     // after setmaxnreg, MMA / TMA / idle warpgroup
+static_assert(kOtherRegs + 2 * kSoftmaxRegs <= 3 * kLaunchRegs, "register split exceeds the launch pool");
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kTmemCols = 512;  // S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D)
 constexpr float kRescaleLog2 = 8.0f;
+#ifndef FA_POLY_PAIRS_PER_8
+#define FA_POLY_PAIRS_PER_8 0
+#endif
+constexpr int kPolyPairsPer8 = FA_POLY_PAIRS_PER_8;  // exp2 column pairs (of 8) computed by polynomial
 constexpr float kLn2 = 0.693147180559945309f;
 
 __host__ __device__ constexpr int item_rows(bool splitk) { return splitk ? kBM : 2 * kBM; }
@@ -252,188 +263,192 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == kLoadWarp) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      uint32_t kv_pos = 0, q_loads = 0;
-      bool ok = true;
-      auto load_kv = [&](const void* tm, int j, int bh) -> bool {
-        const uint32_t s = kv_pos % L::kStages;
-        if (!wait_phase(bar(L::kKVEmpty + s), ((kv_pos / L::kStages) & 1) ^ 1, watch, 1)) return false;
-        mbar_arrive_expect_tx(bar(L::kKVFull + s), L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(kv_addr(s) + c * L::kChunkBytes, tm, bar(L::kKVFull + s), c * 64, j * kBN, bh);
-        ++kv_pos;
-        return true;
-      };
-      for (int k = 0; ok; ++k) {
-        const int t = item_of(k, p.num_items);
-        if (t < 0) break;
-        const Item it = decode_item<CAUSAL>(t, p);
-        int nk, n0, n1;
-        tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
-        // Q tiles: wait until every S MMA of the previous item has read them.
-        if (!(ok = wait_phase(bar(L::kQEmpty), (q_loads & 1) ^ 1, watch, 0))) break;
-        const int nq = (!SPLITK && n1 > 0) ? 2 : 1;
-        mbar_arrive_expect_tx(bar(L::kQFull), nq * L::kTileBytes);
-        for (int i = 0; i < nq; ++i)
+  if (warp >= 8) {
+    regs_lower<kOtherRegs>();
+    if (warp == kLoadWarp) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        uint32_t kv_pos = 0, q_loads = 0;
+        bool ok = true;
+        auto load_kv = [&](const void* tm, int j, int bh) -> bool {
+          const uint32_t s = kv_pos % L::kStages;
+          if (!wait_phase(bar(L::kKVEmpty + s), ((kv_pos / L::kStages) & 1) ^ 1, watch, 1)) return false;
+          mbar_arrive_expect_tx(bar(L::kKVFull + s), L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(q_addr(i) + c * L::kChunkBytes, &p.tm_q, bar(L::kQFull), c * 64,
-                        it.mb * kItemRows + i * kBM, it.bh);
-        ++q_loads;
-        // K/V in the MMA warp's consumption order:
-        //   two query tiles: K0 V0 K1 V1 ...      split-K: K0 K1 V0 K2 V1 K3 V2 ...
-        if (!SPLITK) {
-          for (int j = 0; j < nk && ok; ++j) ok = load_kv(&p.tm_k, j, it.bh) && load_kv(&p.tm_v, j, it.bh);
-        } else {
-          ok = load_kv(&p.tm_k, 0, it.bh);
-          for (int j = 0; j < nk && ok; ++j) {
-            if (j + 1 < nk) ok = load_kv(&p.tm_k, j + 1, it.bh);
-            ok = ok && load_kv(&p.tm_v, j, it.bh);
-          }
-        }
-      }
-      if (!ok) {
-        // Let every load already issued land before the CTA can exit.
-        if (q_loads > 0) wait_phase_drain(bar(L::kQFull), (q_loads - 1) & 1);
-        for (uint32_t s = 0; s < static_cast<uint32_t>(L::kStages); ++s) {
-          if (kv_pos <= s) continue;
-          const uint32_t last = kv_pos - 1 - ((kv_pos - 1 - s) % L::kStages);
-          wait_phase_drain(bar(L::kKVFull + s), (last / L::kStages) & 1);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this loop; one elected lane issues each tcgen05 instruction.
-    {
-      const uint32_t leader = elect_one_lane();
-      constexpr uint32_t idesc_s = instr_desc_f16(BF16, kBM, kBN, false);
-      constexpr uint32_t idesc_o = instr_desc_f16(BF16, kBM, D, true);
-      uint32_t kv_pos = 0, items = 0, merges = 0;
-      uint32_t pcnt0 = 0, pcnt1 = 0;  // P hand-offs consumed per warpgroup
-      bool ok = true;
-      auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
-        return __all_sync(0xffffffffu, wait_phase(b, parity, watch, site));
-      };
-      // Next K/V ring slot: wait until TMA has filled it; returns its stage.
-      auto next_slot = [&](uint32_t& stage) -> bool {
-        stage = kv_pos % L::kStages;
-        if (!wait(bar(L::kKVFull + stage), (kv_pos / L::kStages) & 1, 3)) return false;
-        ++kv_pos;
-        tc_fence_after();
-        return true;
-      };
-
-      // Descriptors are built once; per stage / tile / k-step only the 14-bit start-address
-      // field (address >> 4, no carry possible below 256 KB) is advanced.
-      const uint64_t q_desc = smem_desc_sw128(q_addr(0), 16, 1024);
-      const uint64_t k_desc = smem_desc_sw128(kv_addr(0), 16, 1024);
-      const uint64_t v_desc = smem_desc_sw128(kv_addr(0), L::kChunkBytes, 1024);
-      constexpr uint32_t kTileEnc = L::kTileBytes >> 4;
-
-      // S_w = Q_qi K^T into TMEM columns [128 w, 128 w + 128).
-      auto issue_s = [&](int w, int qi, uint32_t stage) {
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(w * kBN);
-        const uint64_t a0 = q_desc + static_cast<uint32_t>(qi) * kTileEnc;
-        const uint64_t b0 = k_desc + stage * kTileEnc;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss_leader(d_tmem, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u, leader);
-        }
-        mma_commit_leader(bar(L::kSFull + w), leader);
-      };
-      // O_w (+)= P_w V; P_w (fp16/bf16, 64 columns) sits in the first half of S_w's columns.
-      // V tile: keys are the K dimension (rows, 128 B apart), D is the N dimension (MN-major):
-      // 8-key groups are 1024 B apart, 64-column chunks kChunkBytes apart (the LBO).
-      auto issue_pv = [&](int w, uint32_t stage, bool accumulate, bool last) -> bool {
-        const uint32_t pc = w ? pcnt1 : pcnt0;
-        if (!wait(bar(L::kPFull + w), pc & 1, 5 + w)) return false;
-        if (w) ++pcnt1;
-        else ++pcnt0;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(2 * kBN + w * D);
-        const uint32_t a_tmem = tmem + static_cast<uint32_t>(w * kBN);
-        const uint64_t b0 = v_desc + stage * kTileEnc;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts_leader(d_tmem, a_tmem + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_o,
-                        (accumulate || kk > 0) ? 1u : 0u, leader);
-        if (last) mma_commit_leader(bar(L::kOFull + w), leader);
-        return true;
-      };
-      auto release = [&](uint32_t stage) { mma_commit_leader(bar(L::kKVEmpty + stage), leader); };
-
-      for (int k = 0; ok; ++k) {
-        const int t = item_of(k, p.num_items);
-        if (t < 0) break;
-        const Item it = decode_item<CAUSAL>(t, p);
-        int nk, n0, n1;
-        tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
-        if (!(ok = wait(bar(L::kQFull), items & 1, 2))) break;
-        uint32_t sk, sv;
-        if (!SPLITK) {
-          // Both query tiles against K0, then per K/V tile j: PV_w(j) and S_w(j+1), w = 0, 1.
-          if (!(ok = next_slot(sk))) break;
-          issue_s(0, 0, sk);
-          if (n1 > 0) issue_s(1, 1, sk);
-          release(sk);
-          for (int j = 0; j < nk && ok; ++j) {
-            if (!(ok = next_slot(sv))) break;
-            bool k_next = false;
-#pragma unroll
-            for (int w = 0; w < 2; ++w) {
-              const int nw = w ? n1 : n0;
-              if (j < nw && !(ok = issue_pv(w, sv, j > 0, j == nw - 1))) break;
-              if (j + 1 < nw) {
-                if (!k_next && !(ok = next_slot(sk))) break;
-                k_next = true;
-                issue_s(w, w, sk);
-              }
+            tma_load_3d(kv_addr(s) + c * L::kChunkBytes, tm, bar(L::kKVFull + s), c * 64, j * kBN, bh);
+          ++kv_pos;
+          return true;
+        };
+        for (int k = 0; ok; ++k) {
+          const int t = item_of(k, p.num_items);
+          if (t < 0) break;
+          const Item it = decode_item<CAUSAL>(t, p);
+          int nk, n0, n1;
+          tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
+          // Q tiles: wait until every S MMA of the previous item has read them.
+          if (!(ok = wait_phase(bar(L::kQEmpty), (q_loads & 1) ^ 1, watch, 0))) break;
+          const int nq = (!SPLITK && n1 > 0) ? 2 : 1;
+          mbar_arrive_expect_tx(bar(L::kQFull), nq * L::kTileBytes);
+          for (int i = 0; i < nq; ++i)
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_3d(q_addr(i) + c * L::kChunkBytes, &p.tm_q, bar(L::kQFull), c * 64,
+                          it.mb * kItemRows + i * kBM, it.bh);
+          ++q_loads;
+          // K/V in the MMA warp's consumption order:
+          //   two query tiles: K0 V0 K1 V1 ...      split-K: K0 K1 V0 K2 V1 K3 V2 ...
+          if (!SPLITK) {
+            for (int j = 0; j < nk && ok; ++j) ok = load_kv(&p.tm_k, j, it.bh) && load_kv(&p.tm_v, j, it.bh);
+          } else {
+            ok = load_kv(&p.tm_k, 0, it.bh);
+            for (int j = 0; j < nk && ok; ++j) {
+              if (j + 1 < nk) ok = load_kv(&p.tm_k, j + 1, it.bh);
+              ok = ok && load_kv(&p.tm_v, j, it.bh);
             }
-            if (!ok) break;
-            release(sv);
-            if (k_next) release(sk);
           }
-        } else {
-          // One query tile; K/V tile j belongs to warpgroup j & 1.
-          //   S_0(K0), S_1(K1), then per j: PV_{j&1}(V_j), S_{j&1}(K_{j+2}).
-          if (!(ok = next_slot(sk))) break;
-          issue_s(0, 0, sk);
-          release(sk);
-          if (nk > 1) {
+        }
+        if (!ok) {
+          // Let every load already issued land before the CTA can exit.
+          if (q_loads > 0) wait_phase_drain(bar(L::kQFull), (q_loads - 1) & 1);
+          for (uint32_t s = 0; s < static_cast<uint32_t>(L::kStages); ++s) {
+            if (kv_pos <= s) continue;
+            const uint32_t last = kv_pos - 1 - ((kv_pos - 1 - s) % L::kStages);
+            wait_phase_drain(bar(L::kKVFull + s), (last / L::kStages) & 1);
+          }
+        }
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ------------------------------------------------------------ MMA issuer
+      // The whole warp runs this loop; one elected lane issues each tcgen05 instruction.
+      {
+        const uint32_t leader = elect_one_lane();
+        constexpr uint32_t idesc_s = instr_desc_f16(BF16, kBM, kBN, false);
+        constexpr uint32_t idesc_o = instr_desc_f16(BF16, kBM, D, true);
+        uint32_t kv_pos = 0, items = 0, merges = 0;
+        uint32_t pcnt0 = 0, pcnt1 = 0;  // P hand-offs consumed per warpgroup
+        bool ok = true;
+        auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
+          return __all_sync(0xffffffffu, wait_phase(b, parity, watch, site));
+        };
+        // Next K/V ring slot: wait until TMA has filled it; returns its stage.
+        auto next_slot = [&](uint32_t& stage) -> bool {
+          stage = kv_pos % L::kStages;
+          if (!wait(bar(L::kKVFull + stage), (kv_pos / L::kStages) & 1, 3)) return false;
+          ++kv_pos;
+          tc_fence_after();
+          return true;
+        };
+
+        // Descriptors are built once; per stage / tile / k-step only the 14-bit start-address
+        // field (address >> 4, no carry possible below 256 KB) is advanced.
+        const uint64_t q_desc = smem_desc_sw128(q_addr(0), 16, 1024);
+        const uint64_t k_desc = smem_desc_sw128(kv_addr(0), 16, 1024);
+        const uint64_t v_desc = smem_desc_sw128(kv_addr(0), L::kChunkBytes, 1024);
+        constexpr uint32_t kTileEnc = L::kTileBytes >> 4;
+
+        // S_w = Q_qi K^T into TMEM columns [128 w, 128 w + 128).
+        auto issue_s = [&](int w, int qi, uint32_t stage) {
+          const uint32_t d_tmem = tmem + static_cast<uint32_t>(w * kBN);
+          const uint64_t a0 = q_desc + static_cast<uint32_t>(qi) * kTileEnc;
+          const uint64_t b0 = k_desc + stage * kTileEnc;
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+            mma_ss_leader(d_tmem, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u, leader);
+          }
+          mma_commit_leader(bar(L::kSFull + w), leader);
+        };
+        // O_w (+)= P_w V; P_w (fp16/bf16, 64 columns) sits in the first half of S_w's columns.
+        // V tile: keys are the K dimension (rows, 128 B apart), D is the N dimension (MN-major):
+        // 8-key groups are 1024 B apart, 64-column chunks kChunkBytes apart (the LBO).
+        auto issue_pv = [&](int w, uint32_t stage, bool accumulate, bool last) -> bool {
+          const uint32_t pc = w ? pcnt1 : pcnt0;
+          if (!wait(bar(L::kPFull + w), pc & 1, 5 + w)) return false;
+          if (w) ++pcnt1;
+          else ++pcnt0;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + static_cast<uint32_t>(2 * kBN + w * D);
+          const uint32_t a_tmem = tmem + static_cast<uint32_t>(w * kBN);
+          const uint64_t b0 = v_desc + stage * kTileEnc;
+  #pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts_leader(d_tmem, a_tmem + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_o,
+                          (accumulate || kk > 0) ? 1u : 0u, leader);
+          if (last) mma_commit_leader(bar(L::kOFull + w), leader);
+          return true;
+        };
+        auto release = [&](uint32_t stage) { mma_commit_leader(bar(L::kKVEmpty + stage), leader); };
+
+        for (int k = 0; ok; ++k) {
+          const int t = item_of(k, p.num_items);
+          if (t < 0) break;
+          const Item it = decode_item<CAUSAL>(t, p);
+          int nk, n0, n1;
+          tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
+          if (!(ok = wait(bar(L::kQFull), items & 1, 2))) break;
+          uint32_t sk, sv;
+          if (!SPLITK) {
+            // Both query tiles against K0, then per K/V tile j: PV_w(j) and S_w(j+1), w = 0, 1.
             if (!(ok = next_slot(sk))) break;
-            issue_s(1, 0, sk);
+            issue_s(0, 0, sk);
+            if (n1 > 0) issue_s(1, 1, sk);
             release(sk);
-          }
-          for (int j = 0; j < nk && ok; ++j) {
-            const int w = j & 1;
-            if (!(ok = next_slot(sv))) break;
-            // O1 is overwritten by the first PV of warpgroup 1: the previous item's merge
-            // must have read it.
-            if (j == 1 && merges > 0 && !(ok = wait(bar(L::kO1Free), (merges - 1) & 1, 13))) break;
-            if (!(ok = issue_pv(w, sv, j >= 2, j + 2 >= nk))) break;
-            release(sv);
-            if (j + 2 < nk) {
+            for (int j = 0; j < nk && ok; ++j) {
+              if (!(ok = next_slot(sv))) break;
+              bool k_next = false;
+  #pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                const int nw = w ? n1 : n0;
+                if (j < nw && !(ok = issue_pv(w, sv, j > 0, j == nw - 1))) break;
+                if (j + 1 < nw) {
+                  if (!k_next && !(ok = next_slot(sk))) break;
+                  k_next = true;
+                  issue_s(w, w, sk);
+                }
+              }
+              if (!ok) break;
+              release(sv);
+              if (k_next) release(sk);
+            }
+          } else {
+            // One query tile; K/V tile j belongs to warpgroup j & 1.
+            //   S_0(K0), S_1(K1), then per j: PV_{j&1}(V_j), S_{j&1}(K_{j+2}).
+            if (!(ok = next_slot(sk))) break;
+            issue_s(0, 0, sk);
+            release(sk);
+            if (nk > 1) {
               if (!(ok = next_slot(sk))) break;
-              issue_s(w, 0, sk);
+              issue_s(1, 0, sk);
               release(sk);
             }
+            for (int j = 0; j < nk && ok; ++j) {
+              const int w = j & 1;
+              if (!(ok = next_slot(sv))) break;
+              // O1 is overwritten by the first PV of warpgroup 1: the previous item's merge
+              // must have read it.
+              if (j == 1 && merges > 0 && !(ok = wait(bar(L::kO1Free), (merges - 1) & 1, 13))) break;
+              if (!(ok = issue_pv(w, sv, j >= 2, j + 2 >= nk))) break;
+              release(sv);
+              if (j + 2 < nk) {
+                if (!(ok = next_slot(sk))) break;
+                issue_s(w, 0, sk);
+                release(sk);
+              }
+            }
+            if (ok && n1 > 0) ++merges;
           }
-          if (ok && n1 > 0) ++merges;
+          if (!ok) break;
+          mma_commit_leader(bar(L::kQEmpty), leader);
+          ++items;
         }
-        if (!ok) break;
-        mma_commit_leader(bar(L::kQEmpty), leader);
-        ++items;
+        // Whatever happened, wait for every issued MMA before TMEM can be freed.
+        mma_commit_leader(bar(L::kDrain), leader);
+        if (leader) wait_phase_drain(bar(L::kDrain), 0);
       }
-      // Whatever happened, wait for every issued MMA before TMEM can be freed.
-      mma_commit_leader(bar(L::kDrain), leader);
-      if (leader) wait_phase_drain(bar(L::kDrain), 0);
-    }
-    __syncwarp();
+      __syncwarp();
+    }  // warps 10-11: idle
   } else {
+    regs_raise<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax warpgroups
     const int wg = warp >> 2;        // warpgroup: query tile (two-tile items) or K parity (split-K)
     const int wq = warp & 3;         // TMEM lane quarter accessible to this warp
@@ -481,14 +496,54 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           for (int c = 0; c < kBN; ++c)
             if (c > lim) s[c] = -INFINITY;
         }
-        // Row max of the raw scores (scale > 0, so it commutes with the scaling).
-        float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+        // p = 2^(s * scale * log2 e - m) for the 64 columns of half h, packed to fp16/bf16
+        // pairs and stored as P over the first half of this tile's TMEM columns (P column c
+        // holds elements 2c, 2c+1; S is already in registers). Returns the half's row sum;
+        // four partial sums keep the dependency chains short.
+        auto exp_half = [&](float m, int h) -> float {
+          const uint64_t sl2x2 = f2_pack(sl2, sl2);
+          const uint64_t negm2 = f2_pack(-m, -m);
+          uint64_t acc[4] = {0, 0, 0, 0};
+          uint32_t pk[kBN / 4];
 #pragma unroll
-        for (int c = 4; c < kBN; c += 4) {
-          mx0 = max3(mx0, s[c], s[c + 1]);
-          mx1 = max3(mx1, s[c + 2], s[c + 3]);
-        }
-        const float x_max = fmaxf(mx0, mx1) * sl2;
+          for (int i = 0; i < kBN / 4; ++i) {
+            const int c = h * (kBN / 4) + i;  // column pair
+            const uint64_t x2 = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm2);
+            float p0, p1;
+            if ((c & 7) < kPolyPairsPer8) {
+              f2_unpack(exp2_poly_x2(x2), p0, p1);
+            } else {
+              float x0, x1;
+              f2_unpack(x2, x0, x1);
+              p0 = ex2_approx(x0);
+              p1 = ex2_approx(x1);
+            }
+            acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+            pk[i] = pack2<BF16>(p0, p1);
+          }
+          tmem_st32x32b_x32(t_s + h * (kBN / 4), pk);
+          float a0, a1, b0, b1, c0, c1, d0, d1;
+          f2_unpack(acc[0], a0, a1);
+          f2_unpack(acc[1], b0, b1);
+          f2_unpack(acc[2], c0, c1);
+          f2_unpack(acc[3], d0, d1);
+          return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+        };
+        // Row max of the raw scores (scale > 0, so it commutes with the scaling), in eight
+        // independent chains of 3-input max.
+        auto row_max = [&]() -> float {
+          float mx[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+          for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+          return fmaxf(fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5])), fmaxf(mx[6], mx[7]));
+        };
+        // Tile max first, then the exponentials against the running max m_used. m_used only
+        // moves when the tile raises it by more than the threshold (then O and l are rescaled).
+        const float x_max = row_max() * sl2;
         float alpha = 1.f;
         bool rescale = false;
         if (jj == 0) {
@@ -499,28 +554,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           l_run *= alpha;
           rescale = true;
         }
-        // p = 2^(s * scale * log2 e - m_used), two lanes per packed FMA / add.
-        const uint64_t sl2x2 = f2_pack(sl2, sl2);
-        const uint64_t negm2 = f2_pack(-m_used, -m_used);
-        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-        uint32_t pk[kBN / 2];
-#pragma unroll
-        for (int c = 0; c < kBN / 2; ++c) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm2), x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          if (c & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
-          else acc0 = f2_add(acc0, f2_pack(p0, p1));
-          pk[c] = pack2<BF16>(p0, p1);
-        }
-        {
-          float a0, a1, b0, b1;
-          f2_unpack(acc0, a0, a1);
-          f2_unpack(acc1, b0, b1);
-          l_run += (a0 + a1) + (b0 + b1);
-        }
-        tmem_st32x32b_x64(t_s, pk);
+        l_run += exp_half(m_used, 0) + exp_half(m_used, 1);
         if (__any_sync(0xffffffffu, rescale)) {
           // O row *= alpha (alpha = 1 for rows that keep their max). The previous PV of this
           // warpgroup has completed: this tile's S was issued after it.

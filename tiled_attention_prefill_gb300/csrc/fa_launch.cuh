@@ -21,6 +21,12 @@ cudaError_t launch_forward(const Params& p, int grid, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
+    // The kernel redistributes its launch registers with setmaxnreg; a smaller launch
+    // allocation than the split assumes would make setmaxnreg.inc wait forever, so refuse.
+    cudaFuncAttributes attr{};
+    e = cudaFuncGetAttributes(&attr, kernel);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * kNumThreads < 128 * (kOtherRegs + 2 * kSoftmaxRegs)) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
