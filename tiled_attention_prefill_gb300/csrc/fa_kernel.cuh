@@ -61,7 +61,21 @@ constexpr int kOtherRegs = 72;     // after setmaxnreg, MMA / TMA / idle warpgro
 static_assert(kOtherRegs + 2 * kSoftmaxRegs <= 3 * kLaunchRegs, "register split exceeds the launch pool");
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
-constexpr int kTmemCols = 512;  // S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D)
+constexpr int kTmemCols = 512;
+
+// TMEM columns (fp32 S and O, packed 16-bit P). D = 128: S0 [0,128) S1 [128,256)
+// O0 [256,384) O1 [384,512), and P_w overwrites the first half of S_w. D = 64: P has
+// columns of its own, S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384) O0 [384,448)
+// O1 [448,512), which lets the next S of a warpgroup be computed while its softmax still
+// runs (see the MMA schedule).
+template <int D>
+struct TmemCols {
+  static constexpr bool kSepP = (D == 64);
+  __host__ __device__ static constexpr uint32_t s(int w) { return static_cast<uint32_t>(w * kBN); }
+  __host__ __device__ static constexpr uint32_t p(int w) { return static_cast<uint32_t>(kSepP ? 2 * kBN + w * (kBN / 2) : w * kBN); }
+  __host__ __device__ static constexpr uint32_t o(int w) { return static_cast<uint32_t>(kSepP ? 3 * kBN + w * D : 2 * kBN + w * D); }
+};
+static_assert(TmemCols<64>::o(1) + 64 <= kTmemCols && TmemCols<128>::o(1) + 128 <= kTmemCols, "TMEM budget");
 constexpr float kRescaleLog2 = 8.0f;
 #ifndef FA_POLY_PAIRS_PER_8
 #define FA_POLY_PAIRS_PER_8 0
@@ -108,7 +122,9 @@ struct SmemLayout {
   static constexpr int kSFull = kKVEmpty + kStages;  // [2] S of warpgroup i is in TMEM
   static constexpr int kPFull = kSFull + 2;          // [2] P of warpgroup i is in TMEM
   static constexpr int kOFull = kPFull + 2;          // [2] last PV of warpgroup i completed
-  static constexpr int kStats = kOFull + 2;          // split-K: warpgroup 1 published (m, l)
+  static constexpr int kSFree = kOFull + 2;          // [2] warpgroup i has read its S (separate-P form)
+  static constexpr int kPVDone = kSFree + 2;         // [2] each PV of warpgroup i completed (separate-P form)
+  static constexpr int kStats = kPVDone + 2;         // split-K: warpgroup 1 published (m, l)
   static constexpr int kO1Free = kStats + 1;         // split-K: warpgroup 0 finished reading O1
   static constexpr int kDrain = kO1Free + 1;
   static constexpr int kNumBars = kDrain + 1;
@@ -212,6 +228,8 @@ __device__ __forceinline__ int item_of(int k, int num_items) {
 template <int D, bool BF16, bool CAUSAL, bool SPLITK>
 __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   using L = SmemLayout<D>;
+  using TC = TmemCols<D>;
+  constexpr bool kSepP = TC::kSepP;
   constexpr int kItemRows = item_rows(SPLITK);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -241,6 +259,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
       mbar_init(bar(L::kSFull + i), 1);
       mbar_init(bar(L::kPFull + i), kBM);
       mbar_init(bar(L::kOFull + i), 1);
+      mbar_init(bar(L::kSFree + i), kBM);
+      mbar_init(bar(L::kPVDone + i), 1);
     }
     mbar_init(bar(L::kStats), kBM);
     mbar_init(bar(L::kO1Free), kBM);
@@ -295,9 +315,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
                           it.mb * kItemRows + i * kBM, it.bh);
           ++q_loads;
           // K/V in the MMA warp's consumption order:
-          //   two query tiles: K0 V0 K1 V1 ...      split-K: K0 K1 V0 K2 V1 K3 V2 ...
-          if (!SPLITK) {
+          //   two query tiles, P in S's columns:   K0 V0 K1 V1 K2 ...
+          //   two query tiles, separate P, and
+          //   split-K, P in S's columns:           K0 K1 V0 K2 V1 K3 V2 ...
+          //   split-K, separate P:                 K0 K1 K2 K3 V0 V1 K4 K5 V2 V3 ...
+          if (!SPLITK && !kSepP) {
             for (int j = 0; j < nk && ok; ++j) ok = load_kv(&p.tm_k, j, it.bh) && load_kv(&p.tm_v, j, it.bh);
+          } else if (SPLITK && kSepP) {
+            ok = load_kv(&p.tm_k, 0, it.bh);
+            if (nk > 1) ok = ok && load_kv(&p.tm_k, 1, it.bh);
+            for (int t2 = 0; t2 < nk && ok; t2 += 2) {
+              if (t2 + 2 < nk) ok = ok && load_kv(&p.tm_k, t2 + 2, it.bh);
+              if (t2 + 3 < nk) ok = ok && load_kv(&p.tm_k, t2 + 3, it.bh);
+              ok = ok && load_kv(&p.tm_v, t2, it.bh);
+              if (t2 + 1 < nk) ok = ok && load_kv(&p.tm_v, t2 + 1, it.bh);
+            }
           } else {
             ok = load_kv(&p.tm_k, 0, it.bh);
             for (int j = 0; j < nk && ok; ++j) {
@@ -348,17 +380,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
 
         // S_w = Q_qi K^T into TMEM columns [128 w, 128 w + 128).
         auto issue_s = [&](int w, int qi, uint32_t stage) {
-          const uint32_t d_tmem = tmem + static_cast<uint32_t>(w * kBN);
+          const uint32_t d_tmem = tmem + TC::s(w);
           const uint64_t a0 = q_desc + static_cast<uint32_t>(qi) * kTileEnc;
           const uint64_t b0 = k_desc + stage * kTileEnc;
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
             mma_ss_leader(d_tmem, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u, leader);
           }
           mma_commit_leader(bar(L::kSFull + w), leader);
         };
-        // O_w (+)= P_w V; P_w (fp16/bf16, 64 columns) sits in the first half of S_w's columns.
+        // O_w (+)= P_w V; P_w is 64 columns of packed fp16/bf16 pairs (TmemCols).
         // V tile: keys are the K dimension (rows, 128 B apart), D is the N dimension (MN-major):
         // 8-key groups are 1024 B apart, 64-column chunks kChunkBytes apart (the LBO).
         auto issue_pv = [&](int w, uint32_t stage, bool accumulate, bool last) -> bool {
@@ -367,14 +399,26 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           if (w) ++pcnt1;
           else ++pcnt0;
           tc_fence_after();
-          const uint32_t d_tmem = tmem + static_cast<uint32_t>(2 * kBN + w * D);
-          const uint32_t a_tmem = tmem + static_cast<uint32_t>(w * kBN);
+          const uint32_t d_tmem = tmem + TC::o(w);
+          const uint32_t a_tmem = tmem + TC::p(w);
           const uint64_t b0 = v_desc + stage * kTileEnc;
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
             mma_ts_leader(d_tmem, a_tmem + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_o,
                           (accumulate || kk > 0) ? 1u : 0u, leader);
+          if (kSepP) mma_commit_leader(bar(L::kPVDone + w), leader);
           if (last) mma_commit_leader(bar(L::kOFull + w), leader);
+          return true;
+        };
+        // Separate-P form: warpgroup w signals kSFree once per tile it processes (also for its
+        // last tile of an item, which has no next S), so the waits name the completion they need:
+        // the hand-back of tile u of the current item is completion tiles_w + u + 1, where tiles_w
+        // counts warpgroup w's tiles in earlier items.
+        uint32_t tiles0 = 0, tiles1 = 0;
+        auto wait_s_free = [&](int w, int u) -> bool {
+          const uint32_t c = (w ? tiles1 : tiles0) + static_cast<uint32_t>(u) + 1;
+          if (!wait(bar(L::kSFree + w), (c - 1) & 1, 14 + w)) return false;
+          tc_fence_after();
           return true;
         };
         auto release = [&](uint32_t stage) { mma_commit_leader(bar(L::kKVEmpty + stage), leader); };
@@ -387,7 +431,70 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
           if (!(ok = wait(bar(L::kQFull), items & 1, 2))) break;
           uint32_t sk, sv;
-          if (!SPLITK) {
+          if (kSepP && !SPLITK) {
+            // Separate P: S_w(j+1) is issued as soon as warpgroup w has read S_w(j), before
+            // PV_w(j), so the tensor core computes the next S while the softmax runs.
+            if (!(ok = next_slot(sk))) break;
+            issue_s(0, 0, sk);
+            if (n1 > 0) issue_s(1, 1, sk);
+            release(sk);
+            for (int j = 0; j < nk && ok; ++j) {
+              bool k_next = false;
+#pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                if (j + 1 < (w ? n1 : n0)) {
+                  if (!(ok = wait_s_free(w, j))) break;
+                  if (!k_next && !(ok = next_slot(sk))) break;
+                  k_next = true;
+                  issue_s(w, w, sk);
+                }
+              }
+              if (!ok) break;
+              if (k_next) release(sk);
+              if (!(ok = next_slot(sv))) break;
+#pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                const int nw = w ? n1 : n0;
+                if (j < nw && !(ok = issue_pv(w, sv, j > 0, j == nw - 1))) break;
+              }
+              if (!ok) break;
+              release(sv);
+            }
+          } else if (kSepP && SPLITK) {
+            // Separate P, one query tile: tile j belongs to warpgroup j & 1. Per round t2
+            // (even tile t2, odd tile t2 + 1): next S of each warpgroup, then both PVs.
+            if (!(ok = next_slot(sk))) break;
+            issue_s(0, 0, sk);
+            release(sk);
+            if (nk > 1) {
+              if (!(ok = next_slot(sk))) break;
+              issue_s(1, 0, sk);
+              release(sk);
+            }
+            for (int t2 = 0; t2 < nk && ok; t2 += 2) {
+#pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                if (t2 + 2 + w < nk) {
+                  if (!(ok = wait_s_free(w, t2 >> 1)) || !(ok = next_slot(sk))) break;
+                  issue_s(w, 0, sk);
+                  release(sk);
+                }
+              }
+              if (!ok) break;
+#pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                if (t2 + w < nk) {
+                  if (!(ok = next_slot(sv))) break;
+                  // O1 is overwritten by the first PV of warpgroup 1: the previous item's merge
+                  // must have read it.
+                  if (w == 1 && t2 == 0 && merges > 0 && !(ok = wait(bar(L::kO1Free), (merges - 1) & 1, 13))) break;
+                  if (!(ok = issue_pv(w, sv, t2 > 0, t2 + w + 2 >= nk))) break;
+                  release(sv);
+                }
+              }
+            }
+            if (ok && n1 > 0) ++merges;
+          } else if (!SPLITK) {
             // Both query tiles against K0, then per K/V tile j: PV_w(j) and S_w(j+1), w = 0, 1.
             if (!(ok = next_slot(sk))) break;
             issue_s(0, 0, sk);
@@ -396,7 +503,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
             for (int j = 0; j < nk && ok; ++j) {
               if (!(ok = next_slot(sv))) break;
               bool k_next = false;
-  #pragma unroll
+#pragma unroll
               for (int w = 0; w < 2; ++w) {
                 const int nw = w ? n1 : n0;
                 if (j < nw && !(ok = issue_pv(w, sv, j > 0, j == nw - 1))) break;
@@ -440,6 +547,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           if (!ok) break;
           mma_commit_leader(bar(L::kQEmpty), leader);
           ++items;
+          tiles0 += static_cast<uint32_t>(n0);
+          tiles1 += static_cast<uint32_t>(n1);
         }
         // Whatever happened, wait for every issued MMA before TMEM can be freed.
         mma_commit_leader(bar(L::kDrain), leader);
@@ -454,11 +563,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
     const int wq = warp & 3;         // TMEM lane quarter accessible to this warp
     const int r = wq * 32 + lane;    // row within the query tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + static_cast<uint32_t>(wg * kBN);
-    const uint32_t t_o = tmem + lane_off + static_cast<uint32_t>(2 * kBN + wg * D);
-    const uint32_t t_o1 = tmem + lane_off + static_cast<uint32_t>(2 * kBN + D);
+    const uint32_t t_s = tmem + lane_off + TC::s(wg);
+    const uint32_t t_p = tmem + lane_off + TC::p(wg);
+    const uint32_t t_o = tmem + lane_off + TC::o(wg);
+    const uint32_t t_o1 = tmem + lane_off + TC::o(1);
     const float sl2 = p.scale_log2;
     uint32_t scnt = 0, ocnt = 0, o1cnt = 0, mcnt = 0;
+  uint32_t p_sent = 0;  // P hand-offs made by this warpgroup = PVs issued for it
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
@@ -486,6 +597,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
         uint32_t sr[kBN];
         tmem_ld32x32b_x128(t_s, sr);
         float* s = reinterpret_cast<float*>(sr);
+        if (kSepP) {
+          // S is in registers: hand its TMEM columns back so the next S can be computed.
+          tc_fence_before();
+          mbar_arrive(bar(L::kSFree + wg));
+        }
+        bool abort_now = false;
 
         const int col0 = j * kBN;
         const bool diag = CAUSAL && j == qt;
@@ -521,7 +638,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
             acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
             pk[i] = pack2<BF16>(p0, p1);
           }
-          tmem_st32x32b_x32(t_s + h * (kBN / 4), pk);
+          if (kSepP && h == 0 && p_sent > 0) {
+            // P has columns of its own: the previous PV must have read them (and finished
+            // with O) before they are overwritten.
+            const bool pv_ok = wait_phase(bar(L::kPVDone + wg), (p_sent - 1) & 1, watch, 15);
+            if (!__all_sync(0xffffffffu, pv_ok)) abort_now = true;
+            tc_fence_after();
+          }
+          tmem_st32x32b_x32(t_p + h * (kBN / 4), pk);
           float a0, a1, b0, b1, c0, c1, d0, d1;
           f2_unpack(acc[0], a0, a1);
           f2_unpack(acc[1], b0, b1);
@@ -557,7 +681,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
         l_run += exp_half(m_used, 0) + exp_half(m_used, 1);
         if (__any_sync(0xffffffffu, rescale)) {
           // O row *= alpha (alpha = 1 for rows that keep their max). The previous PV of this
-          // warpgroup has completed: this tile's S was issued after it.
+          // warpgroup has completed: with P in S's columns this tile's S was issued after it;
+          // with separate P the kPVDone wait above covered it.
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
             uint32_t o[32];
@@ -570,6 +695,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(L::kPFull + wg));
+        ++p_sent;
+        if (abort_now) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) break;
 
