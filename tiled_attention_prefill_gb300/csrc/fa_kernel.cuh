@@ -282,6 +282,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // Everything above touched only this CTA's shared memory and TMEM; the inputs may be
+  // written by the previous kernel on the stream.
+  grid_dependency_wait();
 
   if (warp >= 8) {
     regs_lower<kOtherRegs>();
@@ -798,6 +801,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) grid_launch_dependents();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

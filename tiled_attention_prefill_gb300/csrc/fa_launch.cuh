@@ -31,7 +31,21 @@ cudaError_t launch_forward(const Params& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  kernel<<<grid, kNumThreads, L::kDynamicBytes, stream>>>(p);
+  // Programmatic dependent launch: the kernel may start (barrier init, TMEM allocation,
+  // descriptor prefetch) while the previous kernel on the stream finishes; it waits for that
+  // kernel (griddepcontrol.wait) before touching global memory.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kNumThreads);
+  cfg.dynamicSmemBytes = L::kDynamicBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

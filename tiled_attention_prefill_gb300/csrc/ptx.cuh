@@ -75,6 +75,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Waits until the grids this launch depends on have completed and their writes are visible
+// (no-op without programmatic dependent launch).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets a dependent grid launched with programmatic serialization start its prologue.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- register budget
 // Warpgroup-wide (all 128 threads execute it). The pool is the CTA's launch allocation.
 template <uint32_t N>

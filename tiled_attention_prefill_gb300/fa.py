@@ -104,6 +104,13 @@ def forward_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B:
                                      float(scale), int(bool(causal)), int(dtype), stream or None)
 
 
+def _current_stream_handle(torch, index: int) -> int:
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)  # fast path, present in torch 2.x
+    if raw is not None:
+        return raw(index)
+    return torch.cuda.current_stream(index).cuda_stream
+
+
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, return_lse: bool = True):
     """Attention forward on CUDA tensors [B, H, N, D] (fp16 or bf16, contiguous).
 
@@ -120,23 +127,30 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
         raise ValueError("q, k, v must have the same shape [B, H, N, D]")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
-    if k.device != q.device or v.device != q.device:
+    dev = q.get_device()
+    if k.get_device() != dev or v.get_device() != dev:
         raise ValueError("q, k, v must be on the same device")
     B, H, N, D = q.shape
     if out is None:
         out = torch.empty_like(q)
-    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.device != q.device:
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or out.get_device() != dev:
         raise ValueError("out must be a contiguous tensor like q")
     if lse is None and return_lse:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if lse is not None and (lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous()
-                            or lse.device != q.device):
+                            or lse.get_device() != dev):
         raise ValueError("lse must be a contiguous fp32 tensor [B, H, N]")
     dtype = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
     sc = -1.0 if scale is None else float(scale)
-    with torch.cuda.device(q.device):
-        stream = torch.cuda.current_stream(q.device).cuda_stream
-        rc = forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                         lse.data_ptr() if lse is not None else 0, B, H, N, D, sc, causal, dtype, stream)
-    _check(rc)
+    lib = _lib if _lib is not None else load_library()
+    lse_ptr = lse.data_ptr() if lse is not None else None
+    if dev == torch.cuda.current_device():
+        rc = lib.fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, N, D, sc,
+                            1 if causal else 0, dtype, _current_stream_handle(torch, dev) or None)
+    else:
+        with torch.cuda.device(dev):
+            rc = lib.fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_ptr, B, H, N, D, sc,
+                                1 if causal else 0, dtype, _current_stream_handle(torch, dev) or None)
+    if rc != FA_OK:
+        _check(rc)
     return out, lse
