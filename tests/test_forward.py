@@ -81,7 +81,7 @@ def test_workload_both_decompositions(name, decomposition):
     assert_close(o, lse, ro, rl, w.dtype, name + " " + decomposition)
 
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c3c"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c3c", "p2s512", "p2s1024"])
 def test_workload_full_oracle(name):
     """Every output element of the smaller workloads against the oracle."""
     w = workloads.WORKLOADS[name]

@@ -17,6 +17,12 @@ discusses sequence length n=2048 in fp16, and the 32-head, D=128 setting of
   c3c       same inputs as c3, causal
   c4        B=4 H=16 N=4096  D=128 bf16  causal      Q,K,V ~ N(0,1)
   c5        B=1 H=8  N=16384 D=128 fp16  non-causal  Q,K ~ 4*N(0,1), V ~ U(-1,1)
+  p2s512    B=1 H=32 N=512   D=128 fp16  non-causal  Q,K,V ~ N(0,1)
+  p2s1024   B=1 H=32 N=1024  D=128 fp16  non-causal  Q,K,V ~ N(0,1)
+
+The last two are the second workload shape of "Flash Attention on Android: tiled SGEMM
+with RenderScript" (section "Benchmark results": 32-head attention at head dim 128,
+sequence 512 and 1024); that page measured FP32, this library computes in fp16/bf16.
 
 Recipe: ``torch.Generator('cpu').manual_seed(seed)``; draw q, k, v in that
 order as fp32 (``randn``; v of c5 as ``rand*2-1``), multiply q and k by the
@@ -73,6 +79,10 @@ WORKLOADS = {
                    note="batched prefill: B=4, 16 heads, N=4096, D=128, bf16, causal"),
     "c5": Workload("c5", 1, 8, 16384, 128, "fp16", False, 1005, qk_mult=4.0, v_uniform=True,
                    note="long sequence: 8 heads, N=16384, D=128, fp16, Q,K x4, V~U(-1,1), non-causal"),
+    "p2s512": Workload("p2s512", 1, 32, 512, 128, "fp16", False, 1006,
+                       note="7B-class shape: 32 heads, N=512, D=128, fp16, non-causal"),
+    "p2s1024": Workload("p2s1024", 1, 32, 1024, 128, "fp16", False, 1007,
+                        note="7B-class shape: 32 heads, N=1024, D=128, fp16, non-causal"),
 }
 
 
