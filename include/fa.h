@@ -106,6 +106,15 @@ FA_API int fa_set_watchdog_ns(unsigned long long ns);
 enum fa_decomposition { FA_DECOMP_AUTO = 0, FA_DECOMP_TWO_TILES = 1, FA_DECOMP_SPLIT_KV = 2 };
 FA_API int fa_set_decomposition(int mode);
 
+/*
+ * Test hook for failure detection (process-wide, for launches that follow): when `on` is
+ * nonzero the MMA warp of every CTA first waits on a barrier that nothing arrives on, so the
+ * device-side wait limit (fa_set_watchdog_ns) must run out; the kernel then records a
+ * timeout, drains its in-flight copies and MMAs, frees tensor memory and returns. Outputs of
+ * such launches are not valid. Returns FA_OK.
+ */
+FA_API int fa_debug_force_stall(int on);
+
 /* The cudaError_t value behind the most recent FA_ERR_CUDA returned on this host thread. */
 FA_API int fa_last_cuda_error(void);
 

@@ -33,6 +33,7 @@ constexpr long long kL2SectionBytes = 32ll << 20;  // K+V bytes of the heads kep
 
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_decomposition{FA_DECOMP_AUTO};
+std::atomic<int> g_force_stall{0};
 thread_local int t_last_cuda_error = 0;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -110,7 +111,7 @@ int encode_map(CUtensorMap* map, const void* base, bool bf16, int BH, int N, int
 // call with the same buffers and sizes skips validation and descriptor encoding.
 struct LaunchKey {
   const void* ptr[5];
-  int B, H, N, D, causal, dtype, dev, decomp;
+  int B, H, N, D, causal, dtype, dev, decomp, stall;
   float scale;
   unsigned long long timeout;
   bool operator==(const LaunchKey& o) const { return std::memcmp(this, &o, sizeof(LaunchKey)) == 0; }
@@ -173,6 +174,11 @@ int fa_set_watchdog_ns(unsigned long long ns) {
 int fa_set_decomposition(int mode) {
   if (mode != FA_DECOMP_AUTO && mode != FA_DECOMP_TWO_TILES && mode != FA_DECOMP_SPLIT_KV) return FA_ERR_INVALID_ARG;
   fa::g_decomposition.store(mode);
+  return FA_OK;
+}
+
+int fa_debug_force_stall(int on) {
+  fa::g_force_stall.store(on != 0 ? 1 : 0);
   return FA_OK;
 }
 
@@ -239,6 +245,7 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   key.dtype = dtype;
   key.dev = dev;
   key.decomp = decomp;
+  key.stall = g_force_stall.load(std::memory_order_relaxed);
   key.scale = scale;
   key.timeout = timeout;
   for (int i = 0; i < kCacheSize; ++i) {
@@ -290,6 +297,7 @@ int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
   long long section = kL2SectionBytes / (kv_head_bytes > 0 ? kv_head_bytes : 1);
   p.section = static_cast<int>(section < 1 ? 1 : (section > BH ? BH : section));
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.force_stall = key.stall;
 
   // Grid. Persistent (one CTA per SM, items strided in snake order) unless the items have
   // very unequal cost (causal) and there are several waves of them: then one CTA per item,

@@ -17,8 +17,8 @@
 //       warp  8     tcgen05 MMA issuer (warp-uniform, one elected lane issues) and TMEM owner
 //       warp  9     TMA producer (one thread)
 //       warps 10-11 idle
-//     setmaxnreg moves registers from the third warpgroup (72 each) to the softmax
-//     warpgroups (216 each); 72 + 2 * 216 = 3 * 168, the launch allocation.
+//     setmaxnreg moves registers from the third warpgroup (88 each) to the softmax
+//     warpgroups (208 each); 88 + 2 * 208 = 3 * 168, the launch allocation.
 //   * K and V tiles (128 keys x D) stream through a shared-memory ring filled by TMA
 //     (128-byte swizzle) in exactly the order the MMA warp consumes them.
 //   * S = Q K^T for a warpgroup goes to its own 128 TMEM columns (fp32). The warpgroup reads
@@ -56,8 +56,8 @@ constexpr int kBM = 128;        // query rows per query tile (tcgen05 M)
 constexpr int kBN = 128;        // keys per K/V tile (tcgen05 N of S = QK^T)
 constexpr int kNumThreads = 384;
 constexpr int kLaunchRegs = 168;   // registers per thread at launch (65536 / 384, rounded down to 8)
-constexpr int kSoftmaxRegs = 216;  // after setmaxnreg, softmax warpgroups
-constexpr int kOtherRegs = 72;     // after setmaxnreg, MMA / TMA / idle warpgroup
+constexpr int kSoftmaxRegs = 208;  // after setmaxnreg, softmax warpgroups
+constexpr int kOtherRegs = 88;     // after setmaxnreg, MMA / TMA / idle warpgroup
 static_assert(kOtherRegs + 2 * kSoftmaxRegs <= 3 * kLaunchRegs, "register split exceeds the launch pool");
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
@@ -102,6 +102,7 @@ struct Params {
   int num_items;               // BH * num_mb
   int section;                 // causal ordering: heads per L2 section
   float scale_log2;            // scale * log2(e)
+  int force_stall;             // test hook: the MMA warp first waits on a barrier nothing arrives on
 };
 
 template <int D>
@@ -126,7 +127,8 @@ struct SmemLayout {
   static constexpr int kPVDone = kSFree + 2;         // [2] each PV of warpgroup i completed (separate-P form)
   static constexpr int kStats = kPVDone + 2;         // split-K: warpgroup 1 published (m, l)
   static constexpr int kO1Free = kStats + 1;         // split-K: warpgroup 0 finished reading O1
-  static constexpr int kDrain = kO1Free + 1;
+  static constexpr int kStall = kO1Free + 1;         // never arrived on (watchdog test hook)
+  static constexpr int kDrain = kStall + 1;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
@@ -264,6 +266,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
     }
     mbar_init(bar(L::kStats), kBM);
     mbar_init(bar(L::kO1Free), kBM);
+    mbar_init(bar(L::kStall), 1);
     mbar_init(bar(L::kDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -382,6 +385,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
         constexpr uint32_t kTileEnc = L::kTileBytes >> 4;
 
         // S_w = Q_qi K^T into TMEM columns [128 w, 128 w + 128).
+        // Q is released as soon as the item's last S MMA has been issued (its completion then
+        // covers every MMA that reads Q), so the next item's Q load overlaps this item's tail.
+        int s_left = 0;  // S MMAs of the current item not yet issued
         auto issue_s = [&](int w, int qi, uint32_t stage) {
           const uint32_t d_tmem = tmem + TC::s(w);
           const uint64_t a0 = q_desc + static_cast<uint32_t>(qi) * kTileEnc;
@@ -392,6 +398,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
             mma_ss_leader(d_tmem, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u, leader);
           }
           mma_commit_leader(bar(L::kSFull + w), leader);
+          if (--s_left == 0) mma_commit_leader(bar(L::kQEmpty), leader);
         };
         // O_w (+)= P_w V; P_w is 64 columns of packed fp16/bf16 pairs (TmemCols).
         // V tile: keys are the K dimension (rows, 128 B apart), D is the N dimension (MN-major):
@@ -426,12 +433,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
         };
         auto release = [&](uint32_t stage) { mma_commit_leader(bar(L::kKVEmpty + stage), leader); };
 
+        if (p.force_stall) ok = wait(bar(L::kStall), 0, 12);  // runs out: exercises the abort path
         for (int k = 0; ok; ++k) {
           const int t = item_of(k, p.num_items);
           if (t < 0) break;
           const Item it = decode_item<CAUSAL>(t, p);
           int nk, n0, n1;
           tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
+          s_left = SPLITK ? nk : n0 + n1;
           if (!(ok = wait(bar(L::kQFull), items & 1, 2))) break;
           uint32_t sk, sv;
           if (kSepP && !SPLITK) {
@@ -548,7 +557,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
             if (ok && n1 > 0) ++merges;
           }
           if (!ok) break;
-          mma_commit_leader(bar(L::kQEmpty), leader);
           ++items;
           tiles0 += static_cast<uint32_t>(n0);
           tiles1 += static_cast<uint32_t>(n1);
@@ -754,26 +762,31 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
       const float inv_l = 1.0f / l_run;
       const float c_self = a_self * inv_l, c_other = a_other * inv_l;
       const uint32_t ob = o_addr(wg);
+      // Columns per step: 64 (one 128-byte swizzle chunk) at D = 64; 32 at D = 128, where the
+      // merge would otherwise hold two 64-column O rows at once.
+      constexpr int kEpi = (D == 64) ? 64 : 32;
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32x32b_x32(t_o + c, o);
+      for (int c = 0; c < D; c += kEpi) {
+        uint32_t o[kEpi];
         if (merge) {
-          uint32_t o1[32];
-          tmem_ld32x32b_x32(t_o1 + c, o1);
+          uint32_t o1[kEpi];
+          if constexpr (kEpi == 64) tmem_ld32x32b_x64_pair(t_o + c, t_o1 + c, o, o1);
+          else tmem_ld32x32b_x32_pair(t_o + c, t_o1 + c, o, o1);
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
+          for (int e = 0; e < kEpi; ++e)
             o[e] = __float_as_uint(__uint_as_float(o[e]) * c_self + __uint_as_float(o1[e]) * c_other);
         } else {
+          if constexpr (kEpi == 64) tmem_ld32x32b_x64(t_o + c, o);
+          else tmem_ld32x32b_x32(t_o + c, o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c_self);
+          for (int e = 0; e < kEpi; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c_self);
         }
+        // 16-byte units (8 columns) of the 128-byte swizzled row of the 64-column chunk.
+        const uint32_t row_base = ob + (c >> 6) * L::kChunkBytes + r * 128;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int col = c + 8 * u;         // first of the 8 columns in this 16-byte unit
-          const int chunk = col >> 6;        // 64-column swizzle chunk
-          const int unit = (col & 63) >> 3;  // 16-byte unit within the 128-byte row
-          const uint32_t addr = ob + chunk * L::kChunkBytes + r * 128 + ((unit ^ (r & 7)) << 4);
+        for (int u = 0; u < kEpi / 8; ++u) {
+          const int unit = ((c & 63) >> 3) + u;
+          const uint32_t addr = row_base + ((unit ^ (r & 7)) << 4);
           const uint32_t w0 = pack2<BF16>(__uint_as_float(o[8 * u + 0]), __uint_as_float(o[8 * u + 1]));
           const uint32_t w1 = pack2<BF16>(__uint_as_float(o[8 * u + 2]), __uint_as_float(o[8 * u + 3]));
           const uint32_t w2 = pack2<BF16>(__uint_as_float(o[8 * u + 4]), __uint_as_float(o[8 * u + 5]));

@@ -39,6 +39,7 @@ SIGNATURES = {
     "fa_set_watchdog_ns": (ctypes.c_int, [ctypes.c_ulonglong]),
     "fa_last_cuda_error": (ctypes.c_int, []),
     "fa_set_decomposition": (ctypes.c_int, [ctypes.c_int]),
+    "fa_debug_force_stall": (ctypes.c_int, [ctypes.c_int]),
 }
 
 _lock = threading.Lock()
@@ -95,6 +96,11 @@ def set_watchdog_ns(ns: int) -> None:
 def set_decomposition(mode: int) -> None:
     """Process-wide work decomposition (FA_DECOMP_AUTO / _TWO_TILES / _SPLIT_KV)."""
     _check(load_library().fa_set_decomposition(int(mode)))
+
+
+def debug_force_stall(on: bool) -> None:
+    """Test hook: following launches stall on purpose so the device-side watchdog fires."""
+    _check(load_library().fa_debug_force_stall(1 if on else 0))
 
 
 def forward_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int, N: int, D: int,
