@@ -18,11 +18,16 @@ RenderScript", section "Architecture: tiled attention with RenderScript BLAS":
     O_i  = sum_j exp(s_ij - M_i) v_j / L_i
     lse_i = M_i + ln L_i
 
-Three entry points:
+Entry points:
 
 * ``attention_rows`` / ``attention``: the C implementation
   (``attention_oracle.c``, fp64, OpenMP over rows) for any size, on all rows
   or on a sampled subset of rows.
+* ``attention_keys`` and ``attention_rows(..., key_ranges=...)``: the same
+  definition restricted to a range of keys, the partial result that split-KV
+  work produces (lse = -inf and O = 0 where the range holds no key of J(i)).
+* ``merge_partials`` (``merge.py``): partial results over disjoint key sets
+  combined by the online-softmax update.
 * ``attention_np``: the same definition in numpy, for tiny cases (a second,
   independent writing used to cross-check the C code).
 * ``online_softmax_blockwise``: the pages' tiled recurrence (section "The
@@ -46,6 +51,8 @@ import subprocess
 import threading
 
 import numpy as np
+
+from .merge import merge_partials  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attention_oracle.c")
@@ -84,6 +91,12 @@ def load_library(path: str):
                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
                   ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    f = lib.oracle_attention_rows_keyrange_f64
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
+                  ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     return lib
@@ -110,10 +123,13 @@ def to_f64(x) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
 
 
-def attention_rows(q, k, v, scale: float, causal: bool, rows, nthreads: int = 0, lib=None):
+def attention_rows(q, k, v, scale: float, causal: bool, rows, nthreads: int = 0, lib=None,
+                   key_ranges=None):
     """Oracle on sampled rows. ``rows``: int array [R, 2] of (bh, i) with bh = b*H + h.
 
-    Returns (o [R, D], lse [R]) in fp64.
+    ``key_ranges`` (optional, int [R, 2]): request r uses only the keys j of J(i) with
+    key_ranges[r, 0] <= j < key_ranges[r, 1] (the partial result of that key range; a range
+    with no such key gives o = 0, lse = -inf). Returns (o [R, D], lse [R]) in fp64.
     """
     q64, k64, v64 = to_f64(q), to_f64(k), to_f64(v)
     B, H, N, D = q64.shape
@@ -123,10 +139,18 @@ def attention_rows(q, k, v, scale: float, causal: bool, rows, nthreads: int = 0,
     o = np.empty((R, D), dtype=np.float64)
     lse = np.empty((R,), dtype=np.float64)
     lib = lib if lib is not None else _get_lib()
-    rc = lib.oracle_attention_rows_f64(
-        q64.ctypes.data, k64.ctypes.data, v64.ctypes.data,
-        B * H, N, D, float(scale), int(bool(causal)),
-        rows.ctypes.data, R, o.ctypes.data, lse.ctypes.data, int(nthreads))
+    if key_ranges is None:
+        rc = lib.oracle_attention_rows_f64(
+            q64.ctypes.data, k64.ctypes.data, v64.ctypes.data,
+            B * H, N, D, float(scale), int(bool(causal)),
+            rows.ctypes.data, R, o.ctypes.data, lse.ctypes.data, int(nthreads))
+    else:
+        kr = np.ascontiguousarray(np.asarray(key_ranges, dtype=np.int64).reshape(-1, 2))
+        assert kr.shape[0] == R
+        rc = lib.oracle_attention_rows_keyrange_f64(
+            q64.ctypes.data, k64.ctypes.data, v64.ctypes.data,
+            B * H, N, D, float(scale), int(bool(causal)),
+            rows.ctypes.data, R, kr.ctypes.data, o.ctypes.data, lse.ctypes.data, int(nthreads))
     if rc != 0:
         raise RuntimeError("oracle_attention_rows_f64 failed with code %d" % rc)
     return o, lse
@@ -138,6 +162,19 @@ def attention(q, k, v, scale: float, causal: bool, nthreads: int = 0, lib=None):
     bh, i = np.meshgrid(np.arange(B * H), np.arange(N), indexing="ij")
     rows = np.stack([bh.ravel(), i.ravel()], axis=1)
     o, lse = attention_rows(q, k, v, scale, causal, rows, nthreads=nthreads, lib=lib)
+    return o.reshape(B, H, N, D), lse.reshape(B, H, N)
+
+
+def attention_keys(q, k, v, scale: float, causal: bool, lo: int, hi: int, nthreads: int = 0, lib=None):
+    """Partial result of every row over the keys lo <= j < hi (within J(i)).
+
+    Returns (o [B,H,N,D], lse [B,H,N]) in fp64; rows without a key get o = 0, lse = -inf.
+    """
+    B, H, N, D = tuple(q.shape)
+    bh, i = np.meshgrid(np.arange(B * H), np.arange(N), indexing="ij")
+    rows = np.stack([bh.ravel(), i.ravel()], axis=1)
+    kr = np.tile(np.array([[lo, hi]], dtype=np.int64), (rows.shape[0], 1))
+    o, lse = attention_rows(q, k, v, scale, causal, rows, nthreads=nthreads, lib=lib, key_ranges=kr)
     return o.reshape(B, H, N, D), lse.reshape(B, H, N)
 
 
