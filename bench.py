@@ -259,8 +259,11 @@ def run_fa(args, w):
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     copies_used = {}
 
-    def measure(wl, steps, warmup):
-        """Mean step time (ms) with the inputs cycled over enough copies to defeat L2."""
+    def measure(wl, steps, warmup, splits=None):
+        """Mean step time (ms) with the inputs cycled over enough copies to defeat L2.
+
+        splits: None times fa_forward; an integer times fa_forward_splitkv with that many
+        splits (one workspace, reused by every step in stream order)."""
         q0, k0, v0 = workloads.make_qkv(wl)
         set_bytes = 4 * q0.numel() * q0.element_size() + wl.B * wl.H * wl.N * 4
         n = n_copies(set_bytes)
@@ -270,15 +273,36 @@ def run_fa(args, w):
             q, k, v = (x.to(dev) for x in (q0, k0, v0))
             sets.append((q, k, v, torch.empty_like(q), torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device=dev)))
 
+        ws = None
+        if splits is not None:
+            ws = torch.empty(max(1, fa.splitkv_workspace_bytes(wl.B, wl.H, wl.N, wl.D, splits)), dtype=torch.uint8,
+                             device=dev)
+
         def fwd(i):
             q, k, v, o, lse = sets[i % n]
-            fa.forward(q, k, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse)
+            if splits is None:
+                fa.forward(q, k, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse)
+            else:
+                fa.forward_splitkv(q, k, v, causal=wl.causal, scale=wl.scale, num_splits=splits, workspace=ws,
+                                   out=o, lse=lse)
 
         ms = time_steps(fwd, steps, warmup, stream)
         fa.check_device_status()
         flops = workloads.attention_flops(wl.B, wl.H, wl.N, wl.D, wl.causal)
-        del sets
+        del sets, ws
         return ms, flops
+
+    def measure_merge(wl, splits, steps=20):
+        """The merge kernel alone on partials of this workload's size (HBM-bound): ms, bytes."""
+        P = splits
+        op = torch.randn((P, wl.B, wl.H, wl.N, wl.D), device=dev)
+        lp = torch.randn((P, wl.B, wl.H, wl.N), device=dev)
+        o = torch.empty((wl.B, wl.H, wl.N, wl.D), dtype=torch.float16, device=dev)
+        lo = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device=dev)
+        ms = time_steps(lambda i: fa.merge_partials(op, lp, out=o, lse=lo), steps, 3, stream)
+        nbytes = (op.numel() + lp.numel()) * 4 + o.numel() * 2 + lo.numel() * 4
+        del op, lp, o, lo
+        return ms, nbytes
 
     sampler = ClockSampler(local) if not args.kernel_only else None
     if sampler:
@@ -323,6 +347,17 @@ def run_fa(args, w):
                            "dram_bytes": tr["dram_bytes"] if tr else None,
                            "dram_vs_min": (tr["dram_bytes"] / workloads.min_dram_bytes(wl.B, wl.H, wl.N, wl.D, with_lse=False))
                            if tr else None}
+            # split-KV forward where its automatic split count is above one
+            S = fa.splitkv_num_splits(wl.B, wl.H, wl.N, wl.D, wl.causal)
+            if S > 1:
+                m2, _ = measure(wl, st, 3, splits=S)
+                mm, mb = measure_merge(wl, S)
+                hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+                sweep[name]["splitkv"] = {
+                    "splits": S, "ms_mean": m2, "tflops": f / (m2 * 1e-3) / 1e12,
+                    "frac_of_peak": f / (m2 * 1e-3) / 1e12 / peak_tf, "speedup_vs_fused": m / m2,
+                    "merge_alone": {"ms": mm, "bytes": mb, "gbs": mb / (mm * 1e-3) / 1e9,
+                                    "frac_of_hbm": mb / (mm * 1e-3) / 1e9 / hbm}}
     clocks = sampler.stop() if sampler else None
 
     if rank != 0:

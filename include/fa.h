@@ -29,12 +29,15 @@
 #define FA_API
 #endif
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
 
-/* Element type of Q, K, V and O. Accumulation is always fp32. */
-enum fa_dtype { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1 };
+/* Element type of Q, K, V and O (fp16/bf16), and of partial outputs (also fp32).
+ * Accumulation is always fp32. */
+enum fa_dtype { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1, FA_DTYPE_FP32 = 2 };
 
 /* Return codes. */
 enum fa_status {
@@ -44,7 +47,8 @@ enum fa_status {
   FA_ERR_ALIGN = -3,       /* Q/K/V/O not 16-byte aligned, or LSE not 4-byte aligned */
   FA_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed; see fa_last_cuda_error() */
   FA_ERR_TIMEOUT = -5,     /* a device-side wait exceeded the watchdog limit */
-  FA_ERR_TOO_LARGE = -6    /* sizes exceed the 32-bit index ranges the kernel uses */
+  FA_ERR_TOO_LARGE = -6,   /* sizes exceed the 32-bit index ranges the kernel uses */
+  FA_ERR_WORKSPACE = -7    /* split-KV workspace missing, misaligned or too small */
 };
 
 /*
@@ -72,6 +76,75 @@ enum fa_status {
  */
 FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
                float scale, int causal, int dtype, void* stream);
+
+/*
+ * Split-KV forward and the merge of partial results.
+ *
+ * The keys of attention decompose: if the keys J(i) of row i are split into disjoint sets
+ * K_1..K_S, the partial result of each set, (O_s, lse_s) = the same formulas as above with
+ * j restricted to K_s, combines into the full result by the online-softmax update of
+ * "Android Transformer Optimization: Attention and Mobile GPU Bottlenecks" (section "The
+ * Essence of FlashAttention: Reordering the Computation") applied to whole sets:
+ *
+ *   m = max_s lse_s,   w_s = exp(lse_s - m),   O = sum_s w_s O_s / sum_s w_s,
+ *   LSE = m + ln sum_s w_s,
+ *
+ * where a set with no key (lse_s = -inf) has weight 0 and its O_s is never read.
+ *
+ * fa_forward_splitkv computes the same O and LSE as fa_forward (arguments as there), but
+ * divides the 128-key tiles of every 128-row query tile into num_splits contiguous ranges
+ * and processes each range as its own work item, so that one query tile can occupy several
+ * SMs. That shortens the longest work items (the last query tiles of a causal sequence) and
+ * fills the GPU when B*H*ceil(N/128) is small. Each item writes its partial result to
+ * `workspace`; a second kernel, on the same stream, merges them into O and LSE.
+ *
+ *   num_splits       1..256, or 0 to choose automatically (fa_splitkv_num_splits). With 1
+ *                    split this is fa_forward (the workspace is not used and may be NULL).
+ *   workspace        device memory of at least fa_splitkv_workspace_bytes(B, H, N, D,
+ *                    splits) bytes for the split count used, 256-byte aligned, not
+ *                    overlapping any other argument; owned by the caller; its contents on
+ *                    entry do not matter (nothing in it has to start at zero). Its layout is
+ *                    partial O [splits, B*H, N, D] fp32, then, at the next 256-byte boundary,
+ *                    partial lse [splits, B*H, N] fp32. Range s of the query tile qt (with
+ *                    n = qt + 1 key tiles when causal, else ceil(N/128)) holds the key tiles
+ *                    [s*n/splits, (s+1)*n/splits) (integer division); an empty range has lse
+ *                    -inf and an unspecified O.
+ *   workspace_bytes  its size in bytes.
+ *
+ * Two calls that share a workspace race unless the stream orders them. Returns FA_OK,
+ * FA_ERR_WORKSPACE, or the codes of fa_forward (FA_ERR_INVALID_ARG also for num_splits
+ * outside 0..256 or a workspace overlapping another argument).
+ */
+FA_API int fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                              int D, float scale, int causal, int dtype, int num_splits, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_forward_splitkv needs for `num_splits` (>= 1) splits; 0 for one split
+ * or invalid arguments. Host only. */
+FA_API size_t fa_splitkv_workspace_bytes(int B, int H, int N, int D, int num_splits);
+
+/* The split count fa_forward_splitkv uses when given 0: a cost model of the whole job (item
+ * lengths against the current device's SM count, plus the merge). >= 1, or a negative
+ * fa_status. */
+FA_API int fa_splitkv_num_splits(int B, int H, int N, int D, int causal);
+
+/*
+ * fa_merge_partials — combines num_parts partial results (formula above).
+ *
+ *   o_parts    [num_parts, B, H, N, D] of parts_dtype (FA_DTYPE_FP16, _BF16 or _FP32),
+ *              16-byte aligned; read only.
+ *   lse_parts  [num_parts, B, H, N] fp32 (-inf: the part has no key for that row); read only.
+ *   o          [B, H, N, D] of dtype (FA_DTYPE_FP16 or _BF16), 16-byte aligned; written. Rows
+ *              without a key in any part get 0.
+ *   lse        [B, H, N] fp32 (-inf for rows without a key) or NULL.
+ *   D          64 or 128.
+ *
+ * Asynchronous on `stream`, allocates nothing. Outputs must not overlap inputs. Returns
+ * FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_ALIGN, FA_ERR_TOO_LARGE or
+ * FA_ERR_CUDA.
+ */
+FA_API int fa_merge_partials(const void* o_parts, const float* lse_parts, int num_parts, int parts_dtype, void* o,
+                             float* lse, int B, int H, int N, int D, int dtype, void* stream);
 
 /* Static description of a return code. Never NULL. */
 FA_API const char* fa_error_string(int code);

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_error_strings(lib):
     assert lib.fa_version() == 100
-    for code in (0, -1, -2, -3, -4, -5, -6):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
         s = lib.fa_error_string(code).decode()
         assert s and s != "unknown error code"
     assert lib.fa_error_string(12345).decode() == "unknown error code"
@@ -116,3 +116,60 @@ def test_decomposition_setter(lib):
     assert lib.fa_set_decomposition(3) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_set_decomposition(-1) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_set_decomposition(0) == fa.FA_OK
+
+
+def _align_up(x, a=256):
+    return (x + a - 1) // a * a
+
+
+def test_splitkv_workspace_bytes(lib):
+    for B, H, N, D, S in ((1, 1, 1, 64, 2), (2, 3, 1000, 128, 5), (1, 32, 1024, 64, 256)):
+        rows = B * H * N
+        want = _align_up(S * rows * D * 4) + _align_up(S * rows * 4)
+        assert lib.fa_splitkv_workspace_bytes(B, H, N, D, S) == want
+    assert lib.fa_splitkv_workspace_bytes(1, 1, 128, 64, 1) == 0      # one split: no workspace
+    assert lib.fa_splitkv_workspace_bytes(1, 1, 128, 96, 2) == 0      # unsupported D
+    assert lib.fa_splitkv_workspace_bytes(1, 1, 128, 64, 0) == 0
+    assert lib.fa_splitkv_workspace_bytes(1, 1, 128, 64, 257) == 0
+    assert lib.fa_splitkv_workspace_bytes(0, 1, 128, 64, 2) == 0
+
+
+def _splitkv(lib, S=2, ws=1 << 44, ws_bytes=1 << 30, q=16, **kw):
+    args = dict(k=32, v=48, o=1 << 40, lse=0, B=1, H=1, N=256, D=64, scale=0.125, causal=0, dtype=0)
+    args.update(kw)
+    return lib.fa_forward_splitkv(q or None, args["k"] or None, args["v"] or None, args["o"] or None,
+                                  args["lse"] or None, args["B"], args["H"], args["N"], args["D"], args["scale"],
+                                  args["causal"], args["dtype"], S, ws or None, ws_bytes, None)
+
+
+def test_splitkv_rejects_bad_arguments_before_any_cuda_call(lib):
+    need = lib.fa_splitkv_workspace_bytes(1, 1, 256, 64, 2)
+    assert _splitkv(lib, S=-1) == fa.FA_ERR_INVALID_ARG
+    assert _splitkv(lib, S=257) == fa.FA_ERR_INVALID_ARG
+    assert _splitkv(lib, q=0) == fa.FA_ERR_INVALID_ARG
+    assert _splitkv(lib, D=96) == fa.FA_ERR_UNSUPPORTED
+    assert _splitkv(lib, ws=0) == fa.FA_ERR_WORKSPACE
+    assert _splitkv(lib, ws=(1 << 44) + 16) == fa.FA_ERR_WORKSPACE          # not 256-byte aligned
+    assert _splitkv(lib, ws_bytes=need - 1) == fa.FA_ERR_WORKSPACE
+    assert _splitkv(lib, ws=1 << 40, ws_bytes=need) == fa.FA_ERR_INVALID_ARG  # overlaps o
+    assert _splitkv(lib, ws=0, q=17) == fa.FA_ERR_ALIGN
+
+
+def _merge(lib, op=1 << 40, lp=1 << 41, P=2, pd=2, o=1 << 42, lse=1 << 43, B=1, H=1, N=8, D=64, dtype=0):
+    return lib.fa_merge_partials(op or None, lp or None, P, pd, o or None, lse or None, B, H, N, D, dtype, None)
+
+
+def test_merge_rejects_bad_arguments_before_any_cuda_call(lib):
+    assert _merge(lib, op=0) == fa.FA_ERR_INVALID_ARG
+    assert _merge(lib, lp=0) == fa.FA_ERR_INVALID_ARG
+    assert _merge(lib, o=0) == fa.FA_ERR_INVALID_ARG
+    assert _merge(lib, P=0) == fa.FA_ERR_INVALID_ARG
+    assert _merge(lib, N=0) == fa.FA_ERR_INVALID_ARG
+    assert _merge(lib, D=96) == fa.FA_ERR_UNSUPPORTED
+    assert _merge(lib, pd=3) == fa.FA_ERR_UNSUPPORTED
+    assert _merge(lib, dtype=2) == fa.FA_ERR_UNSUPPORTED                   # fp32 output not offered
+    assert _merge(lib, op=(1 << 40) + 8) == fa.FA_ERR_ALIGN
+    assert _merge(lib, o=(1 << 42) + 8) == fa.FA_ERR_ALIGN
+    assert _merge(lib, lp=(1 << 41) + 2) == fa.FA_ERR_ALIGN
+    assert _merge(lib, o=(1 << 40) + 256) == fa.FA_ERR_INVALID_ARG         # output inside the parts
+    assert _merge(lib, lse=(1 << 41) + 4) == fa.FA_ERR_INVALID_ARG         # lse inside the part lse

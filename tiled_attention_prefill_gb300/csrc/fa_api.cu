@@ -2,14 +2,19 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <queue>
+#include <vector>
 
 #include "fa.h"
 #include "fa_launch.cuh"
+#include "fa_merge.cuh"
 
 namespace fa {
 
@@ -21,6 +26,14 @@ FA_DECLARE_LAUNCH(extern, 128, false, false)
 FA_DECLARE_LAUNCH(extern, 128, false, true)
 FA_DECLARE_LAUNCH(extern, 128, true, false)
 FA_DECLARE_LAUNCH(extern, 128, true, true)
+FA_DECLARE_LAUNCH_PARTIAL(extern, 64, false, false)
+FA_DECLARE_LAUNCH_PARTIAL(extern, 64, false, true)
+FA_DECLARE_LAUNCH_PARTIAL(extern, 64, true, false)
+FA_DECLARE_LAUNCH_PARTIAL(extern, 64, true, true)
+FA_DECLARE_LAUNCH_PARTIAL(extern, 128, false, false)
+FA_DECLARE_LAUNCH_PARTIAL(extern, 128, false, true)
+FA_DECLARE_LAUNCH_PARTIAL(extern, 128, true, false)
+FA_DECLARE_LAUNCH_PARTIAL(extern, 128, true, true)
 
 // Error bits OR-ed in by kernels of this library on the device they ran on.
 __device__ unsigned int g_device_status = 0;
@@ -30,6 +43,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 constexpr long long kL2SectionBytes = 32ll << 20;  // K+V bytes of the heads kept close in time
+constexpr int kMaxSplits = 256;                    // split-KV ranges per query tile
+constexpr size_t kWorkspaceAlign = 256;
 
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_decomposition{FA_DECOMP_AUTO};
@@ -107,13 +122,28 @@ int encode_map(CUtensorMap* map, const void* base, bool bf16, int BH, int N, int
   return FA_OK;
 }
 
+// Split-KV partial O: fp32 [planes, N, D] viewed as 3-D (D, N, planes); box (32, 32, 1), i.e.
+// 32 rows of 128 bytes, 128-byte swizzle.
+int encode_map_f32(CUtensorMap* map, void* base, long long planes, int N, int D) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(planes)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(N) * D * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return FA_OK;
+}
+
 // Launch parameters (tensor maps included) of recent calls on this host thread: a repeated
 // call with the same buffers and sizes skips validation and descriptor encoding.
 struct LaunchKey {
-  const void* ptr[5];
-  int B, H, N, D, causal, dtype, dev, decomp, stall;
+  const void* ptr[6];  // q, k, v, o, lse, workspace
+  int B, H, N, D, causal, dtype, dev, decomp, stall, splits;
   float scale;
   unsigned long long timeout;
+  size_t workspace_bytes;
   bool operator==(const LaunchKey& o) const { return std::memcmp(this, &o, sizeof(LaunchKey)) == 0; }
 };
 struct LaunchEntry {
@@ -121,6 +151,11 @@ struct LaunchEntry {
   Params params;
   int grid;
   bool splitk;
+  int splits;      // > 1: split-KV partial kernel, then the merge
+  void* o;         // merge output
+  float* lse;
+  long long rows;  // BH * N
+  int num_sms;
   bool valid;
 };
 constexpr int kCacheSize = 4;
@@ -130,6 +165,15 @@ thread_local int t_cache_next = 0;
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
+}
+
+cudaError_t launch_partial(const Params& p, int grid, int D, bool bf16, bool c, cudaStream_t s) {
+  if (D == 64) {
+    if (!bf16) return c ? launch_forward<64, false, true, true, true>(p, grid, s) : launch_forward<64, false, false, true, true>(p, grid, s);
+    return c ? launch_forward<64, true, true, true, true>(p, grid, s) : launch_forward<64, true, false, true, true>(p, grid, s);
+  }
+  if (!bf16) return c ? launch_forward<128, false, true, true, true>(p, grid, s) : launch_forward<128, false, false, true, true>(p, grid, s);
+  return c ? launch_forward<128, true, true, true, true>(p, grid, s) : launch_forward<128, true, false, true, true>(p, grid, s);
 }
 
 cudaError_t launch(const Params& p, int grid, bool splitk, int D, bool bf16, bool c, cudaStream_t s) {
@@ -142,6 +186,228 @@ cudaError_t launch(const Params& p, int grid, bool splitk, int D, bool bf16, boo
   if (!bf16) return c ? FA_LAUNCH(128, false, true) : FA_LAUNCH(128, false, false);
   return c ? FA_LAUNCH(128, true, true) : FA_LAUNCH(128, true, false);
 #undef FA_LAUNCH
+}
+
+// Split-KV workspace: partial O [splits, BH, N, D] fp32, then partial lse [splits, BH, N] fp32,
+// each starting on a kWorkspaceAlign boundary.
+size_t workspace_o_bytes(long long BH, int N, int D, int splits) {
+  const size_t b = static_cast<size_t>(splits) * static_cast<size_t>(BH) * static_cast<size_t>(N) * D * sizeof(float);
+  return (b + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign;
+}
+size_t workspace_bytes(long long BH, int N, int D, int splits) {
+  const size_t l = static_cast<size_t>(splits) * static_cast<size_t>(BH) * static_cast<size_t>(N) * sizeof(float);
+  return workspace_o_bytes(BH, N, D, splits) + (l + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign;
+}
+
+// Split count for a split-KV forward: a cost model of the whole job in microseconds. Work
+// items (one query tile and one K/V range) are dealt to the SMs greedily in the kernel's
+// longest-first order; an item costs a fixed overhead plus its K/V tiles. More splits shorten
+// the longest items (causal rows near the end, or too few items to fill the GPU) but add
+// items, partial-result traffic and the merge kernel.
+int choose_splits(long long BH, int N, int D, bool causal, int num_sms) {
+  const int nkt = (N + kBN - 1) / kBN;
+  const long long base_items = BH * nkt;
+  if (base_items >= 4ll * num_sms || nkt < 2) return 1;
+  const double t_tile = D == 64 ? 0.8 : 0.85;  // us per 128 x 128 tile on one SM
+  const double t_item = 3.0;                   // us of per-item prologue / epilogue
+  const double bytes_per_us = 6.0e6;
+  const long long rows = BH * static_cast<long long>(N);
+  double best_t = 0.0;
+  int best = 1;
+  const int max_s = std::min(16, nkt);
+  std::vector<double> costs;
+  for (int S = 1; S <= max_s; ++S) {
+    costs.clear();
+    for (int qt = 0; qt < nkt; ++qt) {
+      const int nk = causal ? qt + 1 : nkt;
+      for (int sp = 0; sp < S; ++sp) {
+        const int n = (sp + 1) * nk / S - sp * nk / S;
+        if (n > 0) costs.push_back(t_item + n * t_tile);
+      }
+    }
+    std::sort(costs.begin(), costs.end(), std::greater<double>());
+    std::priority_queue<double, std::vector<double>, std::greater<double>> sm;
+    for (int i = 0; i < num_sms; ++i) sm.push(0.0);
+    double makespan = 0.0;
+    for (long long h = 0; h < BH; ++h) {  // heads interleave; each head's items longest-first
+      for (double c : costs) {
+        const double t = sm.top() + c;
+        sm.pop();
+        sm.push(t);
+        makespan = std::max(makespan, t);
+      }
+    }
+    double t = makespan;
+    if (S > 1) t += 2.0 + (static_cast<double>(S) * rows * D * 4 + static_cast<double>(rows) * D * 2) / bytes_per_us;
+    if (S == 1 || t < best_t) {
+      best_t = t;
+      best = S;
+    }
+  }
+  return best;
+}
+
+// Shared by fa_forward (splits = 1) and fa_forward_splitkv (splits >= 1 after the automatic
+// choice). Validation first, then the per-thread launch cache, then descriptor encoding.
+int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+                 float scale, int causal, int dtype, int splits, void* workspace, size_t ws_bytes, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+  auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+  if (mis16(q) || mis16(k) || mis16(v) || mis16(o)) return FA_ERR_ALIGN;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
+
+  const long long BH = static_cast<long long>(B) * H;
+  const long long num_qt = (static_cast<long long>(N) + kBM - 1) / kBM;  // 128-row query tiles
+  if (N > (1 << 30) || BH > 0x7fffffffll || BH * num_qt > 0x7fffffffll) return FA_ERR_TOO_LARGE;
+  const size_t tensor_bytes = static_cast<size_t>(BH) * N * D * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH) * N * sizeof(float);
+  if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
+      overlaps(o, tensor_bytes, v, tensor_bytes) || (lse && overlaps(o, tensor_bytes, lse, lse_bytes)))
+    return FA_ERR_INVALID_ARG;
+  // Split-KV workspace: present, aligned, large enough, disjoint from the other arguments.
+  auto check_workspace = [&](int S) -> int {
+    if (BH * num_qt * S > 0x7fffffffll) return FA_ERR_TOO_LARGE;
+    const size_t need = workspace_bytes(BH, N, D, S);
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kWorkspaceAlign - 1)) != 0 ||
+        ws_bytes < need)
+      return FA_ERR_WORKSPACE;
+    if (overlaps(workspace, need, q, tensor_bytes) || overlaps(workspace, need, k, tensor_bytes) ||
+        overlaps(workspace, need, v, tensor_bytes) || overlaps(workspace, need, o, tensor_bytes) ||
+        (lse && overlaps(workspace, need, lse, lse_bytes)))
+      return FA_ERR_INVALID_ARG;
+    return FA_OK;
+  };
+  int rc = FA_OK;
+  if (splits > 1 && (rc = check_workspace(splits)) != FA_OK) return rc;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  const int decomp = g_decomposition.load(std::memory_order_relaxed);
+  const unsigned long long timeout = g_timeout_ns.load(std::memory_order_relaxed);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  LaunchKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.ptr[0] = q;
+  key.ptr[1] = k;
+  key.ptr[2] = v;
+  key.ptr[3] = o;
+  key.ptr[4] = lse;
+  key.ptr[5] = splits != 1 ? workspace : nullptr;
+  key.B = B;
+  key.H = H;
+  key.N = N;
+  key.D = D;
+  key.causal = causal != 0;
+  key.dtype = dtype;
+  key.dev = dev;
+  key.decomp = decomp;
+  key.stall = g_force_stall.load(std::memory_order_relaxed);
+  key.splits = splits;
+  key.scale = scale;
+  key.timeout = timeout;
+  key.workspace_bytes = splits != 1 ? ws_bytes : 0;
+  for (int i = 0; i < kCacheSize; ++i) {
+    const LaunchEntry& c = t_cache[i];
+    if (c.valid && c.key == key) {
+      if (c.splits > 1) {
+        e = launch_partial(c.params, c.grid, D, bf16, key.causal != 0, s);
+        if (e == cudaSuccess)
+          e = launch_merge(c.params.o_part, kPartsF32, c.params.lse_part, c.splits, c.rows, D, c.o, bf16, c.lse,
+                           c.num_sms, s);
+      } else {
+        e = launch(c.params, c.grid, c.splitk, D, bf16, key.causal != 0, s);
+      }
+      return e == cudaSuccess ? FA_OK : cuda_fail(e);
+    }
+  }
+
+  DeviceInfo* info = nullptr;
+  if ((rc = device_setup(dev, info)) != FA_OK) return rc;
+  if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
+  if (splits == 0) {
+    splits = choose_splits(BH, N, D, causal != 0, info->num_sms);
+    if (splits > 1 && (rc = check_workspace(splits)) != FA_OK) return rc;
+  }
+
+  // Work decomposition. Two query tiles per item halve the K/V traffic per query row; when
+  // that leaves too few items to fill the GPU (short or few sequences), each item is a single
+  // query tile whose K/V range is split between the two softmax warpgroups instead. The
+  // split-KV partial form always uses single query tiles.
+  const long long items_two = BH * ((static_cast<long long>(N) + item_rows(false) - 1) / item_rows(false));
+  bool splitk = decomp == FA_DECOMP_SPLIT_KV || splits > 1;
+  if (decomp == FA_DECOMP_AUTO && splits == 1) {
+    if (causal) {
+      // Unequal item costs are balanced by dispatch order; split only when the GPU is not full.
+      splitk = items_two < info->num_sms;
+    } else {
+      // Equal item costs: compare how well each item count fills whole waves of SMs. The
+      // split-KV form pays a few percent for its extra K/V traffic and merge.
+      auto wave_eff = [&](long long n) {
+        const long long waves = (n + info->num_sms - 1) / info->num_sms;
+        return static_cast<double>(n) / static_cast<double>(waves * info->num_sms);
+      };
+      splitk = wave_eff(2 * items_two) * 0.96 > wave_eff(items_two);
+    }
+  }
+
+  Params p{};
+  if ((rc = encode_map(&p.tm_q, q, bf16, static_cast<int>(BH), N, D, kBM)) != FA_OK) return rc;
+  if ((rc = encode_map(&p.tm_k, k, bf16, static_cast<int>(BH), N, D, kBN)) != FA_OK) return rc;
+  if ((rc = encode_map(&p.tm_v, v, bf16, static_cast<int>(BH), N, D, kBN)) != FA_OK) return rc;
+  if ((rc = encode_map(&p.tm_o, o, bf16, static_cast<int>(BH), N, D, 32)) != FA_OK) return rc;
+  p.lse = lse;
+  p.status = info->status_word;
+  p.timeout_ns = timeout;
+  p.BH = static_cast<int>(BH);
+  p.N = N;
+  p.num_mb = static_cast<int>((static_cast<long long>(N) + item_rows(splitk) - 1) / item_rows(splitk));
+  p.num_splits = splits;
+  p.num_items = static_cast<int>(BH * p.num_mb * splits);
+  const long long kv_head_bytes = 2ll * N * D * 2;
+  long long section = kL2SectionBytes / (kv_head_bytes > 0 ? kv_head_bytes : 1);
+  p.section = static_cast<int>(section < 1 ? 1 : (section > BH ? BH : section));
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.force_stall = key.stall;
+  if (splits > 1) {
+    p.o_part = static_cast<float*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + workspace_o_bytes(BH, N, D, splits));
+    if ((rc = encode_map_f32(&p.tm_op, workspace, BH * splits, N, D)) != FA_OK) return rc;
+  }
+
+  // Grid. Persistent (one CTA per SM, items strided in snake order) unless the items have
+  // very unequal cost (causal) and there are several waves of them: then one CTA per item,
+  // dispatched by the hardware in longest-first order, balances better. Split-KV items are
+  // short and even: persistent, so the per-CTA setup is paid once per SM.
+  const bool per_item = causal != 0 && p.num_items > 2 * info->num_sms && splits == 1;
+  const int grid = (per_item || p.num_items < info->num_sms) ? p.num_items : info->num_sms;
+
+  LaunchEntry& slot = t_cache[t_cache_next];
+  t_cache_next = (t_cache_next + 1) % kCacheSize;
+  slot.key = key;
+  slot.params = p;
+  slot.grid = grid;
+  slot.splitk = splitk;
+  slot.splits = splits;
+  slot.o = o;
+  slot.lse = lse;
+  slot.rows = BH * N;
+  slot.num_sms = info->num_sms;
+  slot.valid = true;
+  if (splits > 1) {
+    e = launch_partial(p, grid, D, bf16, causal != 0, s);
+    if (e == cudaSuccess)
+      e = launch_merge(p.o_part, kPartsF32, p.lse_part, splits, BH * N, D, o, bf16, lse, info->num_sms, s);
+  } else {
+    e = launch(p, grid, splitk, D, bf16, causal != 0, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
 }
 
 }  // namespace
@@ -160,6 +426,7 @@ const char* fa_error_string(int code) {
     case FA_ERR_CUDA: return "CUDA call failed (see fa_last_cuda_error)";
     case FA_ERR_TIMEOUT: return "device-side wait exceeded the watchdog limit";
     case FA_ERR_TOO_LARGE: return "sizes exceed the supported index range";
+    case FA_ERR_WORKSPACE: return "split-KV workspace missing, not 256-byte aligned, or smaller than fa_splitkv_workspace_bytes";
     default: return "unknown error code";
   }
 }
@@ -204,117 +471,66 @@ int fa_check_device_status(void) {
 
 int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
                float scale, int causal, int dtype, void* stream) {
-  using namespace fa;
-  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+  return fa::forward_impl(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, 1, nullptr, 0, stream);
+}
+
+int fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                       int D, float scale, int causal, int dtype, int num_splits, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (num_splits < 0 || num_splits > fa::kMaxSplits) return FA_ERR_INVALID_ARG;
+  return fa::forward_impl(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, num_splits, workspace, workspace_bytes,
+                          stream);
+}
+
+size_t fa_splitkv_workspace_bytes(int B, int H, int N, int D, int num_splits) {
+  if (B < 1 || H < 1 || N < 1 || (D != 64 && D != 128) || num_splits < 1 || num_splits > fa::kMaxSplits) return 0;
+  if (num_splits == 1) return 0;
+  return fa::workspace_bytes(static_cast<long long>(B) * H, N, D, num_splits);
+}
+
+int fa_splitkv_num_splits(int B, int H, int N, int D, int causal) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fa::cuda_fail(e);
+  fa::DeviceInfo* info = nullptr;
+  const int rc = fa::device_setup(dev, info);
+  if (rc != FA_OK) return rc;
+  return fa::choose_splits(static_cast<long long>(B) * H, N, D, causal != 0, info->num_sms);
+}
+
+int fa_merge_partials(const void* o_parts, const float* lse_parts, int num_parts, int parts_dtype, void* o,
+                      float* lse, int B, int H, int N, int D, int dtype, void* stream) {
+  using namespace fa;
+  if (o_parts == nullptr || lse_parts == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || num_parts < 1) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
-  auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
-  if (mis16(q) || mis16(k) || mis16(v) || mis16(o)) return FA_ERR_ALIGN;
-  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
-
-  const long long BH = static_cast<long long>(B) * H;
-  const long long num_qt = (static_cast<long long>(N) + kBM - 1) / kBM;  // 128-row query tiles
-  if (N > (1 << 30) || BH > 0x7fffffffll || BH * num_qt > 0x7fffffffll) return FA_ERR_TOO_LARGE;
-  const size_t tensor_bytes = static_cast<size_t>(BH) * N * D * 2;
-  const size_t lse_bytes = static_cast<size_t>(BH) * N * sizeof(float);
-  if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
-      overlaps(o, tensor_bytes, v, tensor_bytes) || (lse && overlaps(o, tensor_bytes, lse, lse_bytes)))
+  if (parts_dtype != FA_DTYPE_FP16 && parts_dtype != FA_DTYPE_BF16 && parts_dtype != FA_DTYPE_FP32)
+    return FA_ERR_UNSUPPORTED;
+  auto mis = [](const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0; };
+  if (mis(o_parts, 16) || mis(o, 16) || mis(lse_parts, 4) || (lse != nullptr && mis(lse, 4))) return FA_ERR_ALIGN;
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (rows > (1ll << 40) || static_cast<long long>(num_parts) * rows > (1ll << 46)) return FA_ERR_TOO_LARGE;
+  const size_t elem = parts_dtype == FA_DTYPE_FP32 ? 4 : 2;
+  const size_t parts_bytes = static_cast<size_t>(num_parts) * rows * D * elem;
+  const size_t plse_bytes = static_cast<size_t>(num_parts) * rows * sizeof(float);
+  const size_t o_bytes = static_cast<size_t>(rows) * D * 2, lse_bytes = static_cast<size_t>(rows) * sizeof(float);
+  if (overlaps(o, o_bytes, o_parts, parts_bytes) || overlaps(o, o_bytes, lse_parts, plse_bytes) ||
+      (lse && (overlaps(lse, lse_bytes, o_parts, parts_bytes) || overlaps(lse, lse_bytes, lse_parts, plse_bytes) ||
+               overlaps(lse, lse_bytes, o, o_bytes))))
     return FA_ERR_INVALID_ARG;
-
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  const bool bf16 = dtype == FA_DTYPE_BF16;
-  const int decomp = g_decomposition.load(std::memory_order_relaxed);
-  const unsigned long long timeout = g_timeout_ns.load(std::memory_order_relaxed);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  LaunchKey key;
-  std::memset(&key, 0, sizeof(key));
-  key.ptr[0] = q;
-  key.ptr[1] = k;
-  key.ptr[2] = v;
-  key.ptr[3] = o;
-  key.ptr[4] = lse;
-  key.B = B;
-  key.H = H;
-  key.N = N;
-  key.D = D;
-  key.causal = causal != 0;
-  key.dtype = dtype;
-  key.dev = dev;
-  key.decomp = decomp;
-  key.stall = g_force_stall.load(std::memory_order_relaxed);
-  key.scale = scale;
-  key.timeout = timeout;
-  for (int i = 0; i < kCacheSize; ++i) {
-    const LaunchEntry& c = t_cache[i];
-    if (c.valid && c.key == key) {
-      e = launch(c.params, c.grid, c.splitk, D, bf16, key.causal != 0, s);
-      return e == cudaSuccess ? FA_OK : cuda_fail(e);
-    }
-  }
-
   DeviceInfo* info = nullptr;
-  int rc = device_setup(dev, info);
+  const int rc = device_setup(dev, info);
   if (rc != FA_OK) return rc;
-  if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(D));
-
-  // Work decomposition. Two query tiles per item halve the K/V traffic per query row; when
-  // that leaves too few items to fill the GPU (short or few sequences), each item is a single
-  // query tile whose K/V range is split between the two softmax warpgroups instead.
-  const long long items_two = BH * ((static_cast<long long>(N) + item_rows(false) - 1) / item_rows(false));
-  bool splitk = decomp == FA_DECOMP_SPLIT_KV;
-  if (decomp == FA_DECOMP_AUTO) {
-    if (causal) {
-      // Unequal item costs are balanced by dispatch order; split only when the GPU is not full.
-      splitk = items_two < info->num_sms;
-    } else {
-      // Equal item costs: compare how well each item count fills whole waves of SMs. The
-      // split-KV form pays a few percent for its extra K/V traffic and merge.
-      auto wave_eff = [&](long long n) {
-        const long long waves = (n + info->num_sms - 1) / info->num_sms;
-        return static_cast<double>(n) / static_cast<double>(waves * info->num_sms);
-      };
-      splitk = wave_eff(2 * items_two) * 0.96 > wave_eff(items_two);
-    }
-  }
-
-  Params p{};
-  if ((rc = encode_map(&p.tm_q, q, bf16, static_cast<int>(BH), N, D, kBM)) != FA_OK) return rc;
-  if ((rc = encode_map(&p.tm_k, k, bf16, static_cast<int>(BH), N, D, kBN)) != FA_OK) return rc;
-  if ((rc = encode_map(&p.tm_v, v, bf16, static_cast<int>(BH), N, D, kBN)) != FA_OK) return rc;
-  if ((rc = encode_map(&p.tm_o, o, bf16, static_cast<int>(BH), N, D, 32)) != FA_OK) return rc;
-  p.lse = lse;
-  p.status = info->status_word;
-  p.timeout_ns = timeout;
-  p.BH = static_cast<int>(BH);
-  p.N = N;
-  p.num_mb = static_cast<int>((static_cast<long long>(N) + item_rows(splitk) - 1) / item_rows(splitk));
-  p.num_items = static_cast<int>(BH * p.num_mb);
-  const long long kv_head_bytes = 2ll * N * D * 2;
-  long long section = kL2SectionBytes / (kv_head_bytes > 0 ? kv_head_bytes : 1);
-  p.section = static_cast<int>(section < 1 ? 1 : (section > BH ? BH : section));
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.force_stall = key.stall;
-
-  // Grid. Persistent (one CTA per SM, items strided in snake order) unless the items have
-  // very unequal cost (causal) and there are several waves of them: then one CTA per item,
-  // dispatched by the hardware in longest-first order, balances better.
-  const bool per_item = causal != 0 && p.num_items > 2 * info->num_sms;
-  const int grid = (per_item || p.num_items < info->num_sms) ? p.num_items : info->num_sms;
-
-  LaunchEntry& slot = t_cache[t_cache_next];
-  t_cache_next = (t_cache_next + 1) % kCacheSize;
-  slot.key = key;
-  slot.params = p;
-  slot.grid = grid;
-  slot.splitk = splitk;
-  slot.valid = true;
-  e = launch(p, grid, splitk, D, bf16, causal != 0, s);
-  if (e != cudaSuccess) return cuda_fail(e);
-  return FA_OK;
+  const int kind = parts_dtype == FA_DTYPE_FP32 ? kPartsF32 : (parts_dtype == FA_DTYPE_BF16 ? kPartsBF16 : kPartsF16);
+  e = launch_merge(o_parts, kind, lse_parts, num_parts, rows, D, o, dtype == FA_DTYPE_BF16, lse, info->num_sms,
+                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
 }  // extern "C"

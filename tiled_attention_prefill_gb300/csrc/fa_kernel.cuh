@@ -103,6 +103,13 @@ struct Params {
   int section;                 // causal ordering: heads per L2 section
   float scale_log2;            // scale * log2(e)
   int force_stall;             // test hook: the MMA warp first waits on a barrier nothing arrives on
+  // Split-KV partial form only: the K/V tiles of every query tile are divided into num_splits
+  // contiguous ranges, one work item each; item results go to o_part [num_splits, BH, N, D]
+  // and lse_part [num_splits, BH, N] (fp32) instead of O and lse.
+  int num_splits;
+  float* o_part;
+  float* lse_part;
+  CUtensorMap tm_op;  // o_part as 3-D fp32 (D, N, num_splits * BH), box (32, 32, 1), 128B swizzle
 };
 
 template <int D>
@@ -172,7 +179,8 @@ __device__ __forceinline__ bool wait_phase_drain(uint32_t bar, uint32_t parity) 
 
 struct Item {
   int bh;
-  int mb;  // row block: 256 rows (two query tiles) or, split-K, one 128-row query tile
+  int mb;     // row block: 256 rows (two query tiles) or, split-K, one 128-row query tile
+  int split;  // split-KV partial form: which K/V range of the query tile
 };
 
 // Work-item order. Non-causal: head-major (all row blocks of a head run close together, so
@@ -216,6 +224,32 @@ __device__ __forceinline__ void tile_counts(int mb, int N, int& nk, int& n0, int
   }
 }
 
+// Work item t: its query rows and its K/V tiles [jb, jb + nk), of which warpgroup w processes
+// n_w (tile_counts). In the split-KV partial form item t is split t % num_splits of row block
+// t / num_splits, whose nk_full tiles are divided as [s nk_full / S, (s + 1) nk_full / S): a
+// range may be empty (nk = 0) when the row block has fewer tiles than splits.
+template <bool CAUSAL, bool SPLITK, bool PARTIAL>
+__device__ __forceinline__ Item decode_work(int t, const Params& p, int& jb, int& nk, int& n0, int& n1) {
+  int s = 0;
+  if (PARTIAL) {
+    s = t % p.num_splits;
+    t /= p.num_splits;
+  }
+  Item it = decode_item<CAUSAL>(t, p);
+  it.split = s;
+  tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
+  jb = 0;
+  if (PARTIAL) {
+    const int lo = s * nk / p.num_splits;
+    const int hi = (s + 1) * nk / p.num_splits;
+    jb = lo;
+    nk = hi - lo;
+    n0 = (nk + 1) >> 1;
+    n1 = nk >> 1;
+  }
+  return it;
+}
+
 // k-th work item of this CTA in snake order over the sorted item list (-1 when done). With
 // one CTA per item (gridDim.x == num_items) this is just blockIdx.x.
 __device__ __forceinline__ int item_of(int k, int num_items) {
@@ -227,8 +261,9 @@ __device__ __forceinline__ int item_of(int k, int num_items) {
   return t < num_items ? static_cast<int>(t) : -1;
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SPLITK>
+template <int D, bool BF16, bool CAUSAL, bool SPLITK, bool PARTIAL>
 __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
+  static_assert(!PARTIAL || SPLITK, "the split-KV partial form uses one query tile per item");
   using L = SmemLayout<D>;
   using TC = TmemCols<D>;
   constexpr bool kSepP = TC::kSepP;
@@ -296,21 +331,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
       if (lane == 0) {
         uint32_t kv_pos = 0, q_loads = 0;
         bool ok = true;
+        int jb = 0;  // first K/V tile of the current item
         auto load_kv = [&](const void* tm, int j, int bh) -> bool {
           const uint32_t s = kv_pos % L::kStages;
           if (!wait_phase(bar(L::kKVEmpty + s), ((kv_pos / L::kStages) & 1) ^ 1, watch, 1)) return false;
           mbar_arrive_expect_tx(bar(L::kKVFull + s), L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(kv_addr(s) + c * L::kChunkBytes, tm, bar(L::kKVFull + s), c * 64, j * kBN, bh);
+            tma_load_3d(kv_addr(s) + c * L::kChunkBytes, tm, bar(L::kKVFull + s), c * 64, (jb + j) * kBN, bh);
           ++kv_pos;
           return true;
         };
         for (int k = 0; ok; ++k) {
           const int t = item_of(k, p.num_items);
           if (t < 0) break;
-          const Item it = decode_item<CAUSAL>(t, p);
           int nk, n0, n1;
-          tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
+          const Item it = decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, jb, nk, n0, n1);
+          if (nk == 0) continue;  // empty split-KV range: nothing to load
           // Q tiles: wait until every S MMA of the previous item has read them.
           if (!(ok = wait_phase(bar(L::kQEmpty), (q_loads & 1) ^ 1, watch, 0))) break;
           const int nq = (!SPLITK && n1 > 0) ? 2 : 1;
@@ -437,9 +473,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
         for (int k = 0; ok; ++k) {
           const int t = item_of(k, p.num_items);
           if (t < 0) break;
-          const Item it = decode_item<CAUSAL>(t, p);
-          int nk, n0, n1;
-          tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
+          int jb, nk, n0, n1;
+          decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, jb, nk, n0, n1);
+          if (nk == 0) continue;  // empty split-KV range
           s_left = SPLITK ? nk : n0 + n1;
           if (!(ok = wait(bar(L::kQFull), items & 1, 2))) break;
           uint32_t sk, sv;
@@ -580,24 +616,29 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
     const uint32_t t_o1 = tmem + lane_off + TC::o(1);
     const float sl2 = p.scale_log2;
     uint32_t scnt = 0, ocnt = 0, o1cnt = 0, mcnt = 0;
-  uint32_t p_sent = 0;  // P hand-offs made by this warpgroup = PVs issued for it
+    uint32_t p_sent = 0;  // P hand-offs made by this warpgroup = PVs issued for it
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
       const int t = item_of(k, p.num_items);
       if (t < 0) break;
-      const Item it = decode_item<CAUSAL>(t, p);
-      int nk, n0, n1;
-      tile_counts<CAUSAL, SPLITK>(it.mb, p.N, nk, n0, n1);
+      int jb, nk, n0, n1;
+      const Item it = decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, jb, nk, n0, n1);
       const int n_mine = wg == 0 ? n0 : n1;
-      if (n_mine == 0) continue;
       const int qt = SPLITK ? it.mb : 2 * it.mb + wg;  // query tile index (its diagonal K tile)
       const int row = qt * kBM + r;                     // query index within the sequence
+      if (PARTIAL && nk == 0) {
+        // Empty K/V range: the partial result has no key (lse = -inf; the merge skips it).
+        if (wg == 0 && row < p.N)
+          p.lse_part[(static_cast<long long>(it.split) * p.BH + it.bh) * p.N + row] = -INFINITY;
+        continue;
+      }
+      if (n_mine == 0) continue;
       float m_used = -INFINITY;
       float l_run = 0.f;
 
       for (int jj = 0; jj < n_mine; ++jj) {
-        const int j = SPLITK ? 2 * jj + wg : jj;  // K/V tile index
+        const int j = jb + (SPLITK ? 2 * jj + wg : jj);  // K/V tile index
         bool w_ok = wait_phase(bar(L::kSFull + wg), scnt & 1, watch, 8 + wg);
         if (!__all_sync(0xffffffffu, w_ok)) {
           ok = false;
@@ -762,6 +803,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
       const float inv_l = 1.0f / l_run;
       const float c_self = a_self * inv_l, c_other = a_other * inv_l;
       const uint32_t ob = o_addr(wg);
+      // Split-KV partial form: warp wq's fp32 boxes go to its quarter of the O staging tile of
+      // warpgroup 0, then to its quarter of the second Q tile (single query tiles leave it unused).
+      auto part_box = [&](int b) -> uint32_t {
+        constexpr int kPerRegion = D / 64;  // 4 KB boxes per quarter tile
+        const uint32_t region = b < kPerRegion ? o_addr(0) : q_addr(1);
+        return region + wq * (L::kTileBytes / 4) + (b % kPerRegion) * 4096;
+      };
       // Columns per step: 64 (one 128-byte swizzle chunk) at D = 64; 32 at D = 128, where the
       // merge would otherwise hold two 64-column O rows at once.
       constexpr int kEpi = (D == 64) ? 64 : 32;
@@ -781,6 +829,19 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
 #pragma unroll
           for (int e = 0; e < kEpi; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c_self);
         }
+        if constexpr (PARTIAL) {
+          // fp32 partial rows: each warp stages its 32 rows as D/32 boxes of 32 rows x 32
+          // columns (128-byte swizzled rows, 4 KB each), then stores them with TMA.
+#pragma unroll
+          for (int u = 0; u < kEpi / 4; ++u) {
+            const int col = c + 4 * u;
+            const uint32_t addr = part_box(col >> 5) + lane * 128 + ((((col & 31) >> 2) ^ (lane & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o[4 * u + 0]),
+                         "r"(o[4 * u + 1]), "r"(o[4 * u + 2]), "r"(o[4 * u + 3])
+                         : "memory");
+          }
+          continue;
+        }
         // 16-byte units (8 columns) of the 128-byte swizzled row of the 64-column chunk.
         const uint32_t row_base = ob + (c >> 6) * L::kChunkBytes + r * 128;
 #pragma unroll
@@ -797,6 +858,19 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
       }
       tc_fence_before();
       if (merge) mbar_arrive(bar(L::kO1Free));  // O1 and (m1, l1) consumed
+      if constexpr (PARTIAL) {
+        if (row < p.N)
+          p.lse_part[(static_cast<long long>(it.split) * p.BH + it.bh) * p.N + row] = (m_used + log2f(l_run)) * kLn2;
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int row0_warp = qt * kBM + wq * 32;
+        if (lane == 0 && row0_warp < p.N) {
+          for (int b = 0; b < D / 32; ++b)
+            tma_store_3d(&p.tm_op, part_box(b), b * 32, row0_warp, it.split * p.BH + it.bh);
+          bulk_commit_group();
+        }
+        continue;
+      }
       if (p.lse != nullptr && row < p.N)
         p.lse[static_cast<long long>(it.bh) * p.N + row] = (m_used + log2f(l_run)) * kLn2;
       fence_proxy_async_smem();

@@ -1,5 +1,5 @@
-// Kernel launcher template, explicitly instantiated in fa_inst_d64.cu / fa_inst_d128.cu so
-// that the eight kernel variants compile in parallel.
+// Kernel launcher template, explicitly instantiated in fa_inst_d64.cu, fa_inst_d128.cu and
+// fa_inst_partial.cu so that the kernel variants compile in parallel.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -10,10 +10,10 @@
 
 namespace fa {
 
-template <int D, bool BF16, bool CAUSAL, bool SPLITK>
+template <int D, bool BF16, bool CAUSAL, bool SPLITK, bool PARTIAL = false>
 cudaError_t launch_forward(const Params& p, int grid, cudaStream_t stream) {
   using L = SmemLayout<D>;
-  auto kernel = fa_fwd_kernel<D, BF16, CAUSAL, SPLITK>;
+  auto kernel = fa_fwd_kernel<D, BF16, CAUSAL, SPLITK, PARTIAL>;
   // Opt in to the large dynamic shared-memory carve-out once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -49,8 +49,10 @@ cudaError_t launch_forward(const Params& p, int grid, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-#define FA_DECLARE_LAUNCH(EXT, D, BF16, CAUSAL)                                                       \
-  EXT template cudaError_t launch_forward<D, BF16, CAUSAL, false>(const Params&, int, cudaStream_t); \
-  EXT template cudaError_t launch_forward<D, BF16, CAUSAL, true>(const Params&, int, cudaStream_t);
+#define FA_DECLARE_LAUNCH(EXT, D, BF16, CAUSAL)                                                              \
+  EXT template cudaError_t launch_forward<D, BF16, CAUSAL, false, false>(const Params&, int, cudaStream_t); \
+  EXT template cudaError_t launch_forward<D, BF16, CAUSAL, true, false>(const Params&, int, cudaStream_t);
+#define FA_DECLARE_LAUNCH_PARTIAL(EXT, D, BF16, CAUSAL) \
+  EXT template cudaError_t launch_forward<D, BF16, CAUSAL, true, true>(const Params&, int, cudaStream_t);
 
 }  // namespace fa

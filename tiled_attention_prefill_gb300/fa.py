@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
 
 FA_DTYPE_FP16 = 0
 FA_DTYPE_BF16 = 1
+FA_DTYPE_FP32 = 2
 FA_OK = 0
 FA_ERR_INVALID_ARG = -1
 FA_ERR_UNSUPPORTED = -2
@@ -24,6 +25,7 @@ FA_ERR_ALIGN = -3
 FA_ERR_CUDA = -4
 FA_ERR_TIMEOUT = -5
 FA_ERR_TOO_LARGE = -6
+FA_ERR_WORKSPACE = -7
 FA_DECOMP_AUTO = 0
 FA_DECOMP_TWO_TILES = 1
 FA_DECOMP_SPLIT_KV = 2
@@ -40,6 +42,16 @@ SIGNATURES = {
     "fa_last_cuda_error": (ctypes.c_int, []),
     "fa_set_decomposition": (ctypes.c_int, [ctypes.c_int]),
     "fa_debug_force_stall": (ctypes.c_int, [ctypes.c_int]),
+    "fa_forward_splitkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                          ctypes.c_size_t, ctypes.c_void_p]),
+    "fa_splitkv_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int]),
+    "fa_splitkv_num_splits": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "fa_merge_partials": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
 }
 
 _lock = threading.Lock()
@@ -159,4 +171,95 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
                                 1 if causal else 0, dtype, _current_stream_handle(torch, dev) or None)
     if rc != FA_OK:
         _check(rc)
+    return out, lse
+
+
+def _check_qkv(torch, q, k, v):
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share dtype fp16 or bf16")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, H, N, D]")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    if k.get_device() != q.get_device() or v.get_device() != q.get_device():
+        raise ValueError("q, k, v must be on the same device")
+
+
+def splitkv_num_splits(B: int, H: int, N: int, D: int, causal: bool) -> int:
+    """Split count ``fa_forward_splitkv`` chooses for num_splits = 0 (needs the device)."""
+    rc = load_library().fa_splitkv_num_splits(int(B), int(H), int(N), int(D), int(bool(causal)))
+    if rc < 0:
+        _check(rc)
+    return rc
+
+
+def splitkv_workspace_bytes(B: int, H: int, N: int, D: int, num_splits: int) -> int:
+    return int(load_library().fa_splitkv_workspace_bytes(int(B), int(H), int(N), int(D), int(num_splits)))
+
+
+def forward_splitkv(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int = 0,
+                    workspace=None, out=None, lse=None, return_lse: bool = True):
+    """Split-KV forward (``fa_forward_splitkv``): same result as :func:`forward`.
+
+    ``num_splits`` 0 lets the library choose. ``workspace`` is a CUDA uint8 tensor of at least
+    ``splitkv_workspace_bytes`` bytes (256-byte aligned); allocated here when None. Returns
+    (o, lse) like :func:`forward`; the workspace afterwards holds the partial results.
+    """
+    import torch
+
+    _check_qkv(torch, q, k, v)
+    B, H, N, D = q.shape
+    dev = q.get_device()
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(dev):
+        splits = num_splits if num_splits > 0 else splitkv_num_splits(B, H, N, D, causal)
+        if workspace is None:
+            nbytes = splitkv_workspace_bytes(B, H, N, D, splits)
+            workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+        dtype = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
+        sc = -1.0 if scale is None else float(scale)
+        rc = load_library().fa_forward_splitkv(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            B, H, N, D, sc, 1 if causal else 0, dtype, int(splits), workspace.data_ptr(), workspace.numel(),
+            _current_stream_handle(torch, dev) or None)
+    _check(rc)
+    return out, lse
+
+
+def merge_partials(o_parts, lse_parts, out_dtype=None, out=None, lse=None):
+    """``fa_merge_partials``: o_parts [P, B, H, N, D] (fp16/bf16/fp32), lse_parts [P, B, H, N] fp32.
+
+    Returns (o [B, H, N, D] in ``out_dtype`` (default: the parts' type, fp16 for fp32 parts),
+    lse [B, H, N] fp32).
+    """
+    import torch
+
+    if o_parts.dim() != 5 or lse_parts.shape != o_parts.shape[:4]:
+        raise ValueError("o_parts [P, B, H, N, D] and lse_parts [P, B, H, N] expected")
+    if not (o_parts.is_cuda and lse_parts.is_cuda and o_parts.is_contiguous() and lse_parts.is_contiguous()):
+        raise ValueError("parts must be contiguous CUDA tensors")
+    if lse_parts.dtype != torch.float32:
+        raise ValueError("lse_parts must be fp32")
+    kinds = {torch.float16: FA_DTYPE_FP16, torch.bfloat16: FA_DTYPE_BF16, torch.float32: FA_DTYPE_FP32}
+    if o_parts.dtype not in kinds:
+        raise ValueError("o_parts must be fp16, bf16 or fp32")
+    P, B, H, N, D = o_parts.shape
+    if out_dtype is None:
+        out_dtype = torch.float16 if o_parts.dtype == torch.float32 else o_parts.dtype
+    if out is None:
+        out = torch.empty((B, H, N, D), dtype=out_dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=o_parts.device)
+    dev = o_parts.get_device()
+    with torch.cuda.device(dev):
+        rc = load_library().fa_merge_partials(
+            o_parts.data_ptr(), lse_parts.data_ptr(), P, kinds[o_parts.dtype], out.data_ptr(), lse.data_ptr(),
+            B, H, N, D, FA_DTYPE_BF16 if out.dtype == torch.bfloat16 else FA_DTYPE_FP16,
+            _current_stream_handle(torch, dev) or None)
+    _check(rc)
     return out, lse

@@ -19,10 +19,15 @@ discusses sequence length n=2048 in fp16, and the 32-head, D=128 setting of
   c5        B=1 H=8  N=16384 D=128 fp16  non-causal  Q,K ~ 4*N(0,1), V ~ U(-1,1)
   p2s512    B=1 H=32 N=512   D=128 fp16  non-causal  Q,K,V ~ N(0,1)
   p2s1024   B=1 H=32 N=1024  D=128 fp16  non-causal  Q,K,V ~ N(0,1)
+  lc1       B=1 H=1  N=16384 D=128 fp16  causal      Q,K,V ~ N(0,1)
 
 The last two are the second workload shape of "Flash Attention on Android: tiled SGEMM
 with RenderScript" (section "Benchmark results": 32-head attention at head dim 128,
 sequence 512 and 1024); that page measured FP32, this library computes in fp16/bf16.
+``lc1`` is one long causal sequence with a single head: 128 query tiles, fewer than the
+GPU's SMs, the longest of them 128 key tiles long. It is the case the split-KV forward
+(partial results over key ranges, merged with the online-softmax update of the first
+page's section "The Essence of FlashAttention: Reordering the Computation") is for.
 
 Recipe: ``torch.Generator('cpu').manual_seed(seed)``; draw q, k, v in that
 order as fp32 (``randn``; v of c5 as ``rand*2-1``), multiply q and k by the
@@ -83,6 +88,8 @@ WORKLOADS = {
                        note="7B-class shape: 32 heads, N=512, D=128, fp16, non-causal"),
     "p2s1024": Workload("p2s1024", 1, 32, 1024, 128, "fp16", False, 1007,
                         note="7B-class shape: 32 heads, N=1024, D=128, fp16, non-causal"),
+    "lc1": Workload("lc1", 1, 1, 16384, 128, "fp16", True, 1008,
+                    note="one long causal sequence: 1 head, N=16384, D=128, fp16"),
 }
 
 
