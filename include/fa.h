@@ -48,7 +48,8 @@ enum fa_status {
   FA_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed; see fa_last_cuda_error() */
   FA_ERR_TIMEOUT = -5,     /* a device-side wait exceeded the watchdog limit */
   FA_ERR_TOO_LARGE = -6,   /* sizes exceed the 32-bit index ranges the kernel uses */
-  FA_ERR_WORKSPACE = -7    /* split-KV workspace missing, misaligned or too small */
+  FA_ERR_WORKSPACE = -7,   /* split-KV workspace missing, misaligned or too small */
+  FA_ERR_SCRATCH = -8      /* split-KV partials larger than the built-in scratch (noalloc) */
 };
 
 /*
@@ -118,6 +119,31 @@ FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, floa
 FA_API int fa_forward_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
                               int D, float scale, int causal, int dtype, int num_splits, void* workspace,
                               size_t workspace_bytes, void* stream);
+
+/*
+ * fa_forward_splitkv_noalloc — fa_forward_splitkv without a caller workspace and without any
+ * allocation: the partial results go to a scratch array that is part of the library's device
+ * code (a static __device__ array of 32 MiB = 33554432 bytes per device, 256-byte aligned).
+ * This entry point is an engineering convenience; the pages have no counterpart to it.
+ *
+ *   arguments   as fa_forward_splitkv, minus workspace and workspace_bytes.
+ *   limit       the split count used (given, or chosen when num_splits is 0) must need at most
+ *               32 MiB, i.e. fa_splitkv_workspace_bytes(B, H, N, D, splits) <= 33554432;
+ *               otherwise FA_ERR_SCRATCH and nothing is enqueued. One split needs no scratch.
+ *   zeroing     nothing in the scratch has to start at zero; every partial that the merge
+ *               reads is written by the same call first.
+ *   setup       the first call on a device does one-time setup (the device checks of
+ *               fa_forward, then cudaGetSymbolAddress of the scratch with that device
+ *               current); make that first call outside any stream capture.
+ *   races       there is one scratch per device: two calls whose execution overlaps (on two
+ *               streams, or from two threads) race on it and give wrong results. Calls
+ *               ordered on one stream are fine.
+ *
+ * Allocates no memory (no cudaMalloc, cudaFree or allocating library call). Returns the codes
+ * of fa_forward_splitkv except FA_ERR_WORKSPACE, plus FA_ERR_SCRATCH.
+ */
+FA_API int fa_forward_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                      int N, int D, float scale, int causal, int dtype, int num_splits, void* stream);
 
 /* Workspace bytes fa_forward_splitkv needs for `num_splits` (>= 1) splits; 0 for one split
  * or invalid arguments. Host only. */

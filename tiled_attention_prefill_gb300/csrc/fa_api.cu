@@ -38,6 +38,11 @@ FA_DECLARE_LAUNCH_PARTIAL(extern, 128, true, true)
 // Error bits OR-ed in by kernels of this library on the device they ran on.
 __device__ unsigned int g_device_status = 0;
 
+// Split-KV scratch of fa_forward_splitkv_noalloc: module memory, so that entry point needs no
+// allocation. One per device; calls that overlap in time on a device share it.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -427,6 +432,7 @@ const char* fa_error_string(int code) {
     case FA_ERR_TIMEOUT: return "device-side wait exceeded the watchdog limit";
     case FA_ERR_TOO_LARGE: return "sizes exceed the supported index range";
     case FA_ERR_WORKSPACE: return "split-KV workspace missing, not 256-byte aligned, or smaller than fa_splitkv_workspace_bytes";
+    case FA_ERR_SCRATCH: return "split-KV partials exceed the built-in 32 MiB scratch of fa_forward_splitkv_noalloc (use fewer splits or fa_forward_splitkv)";
     default: return "unknown error code";
   }
 }
@@ -531,6 +537,43 @@ int fa_merge_partials(const void* o_parts, const float* lse_parts, int num_parts
   e = launch_merge(o_parts, kind, lse_parts, num_parts, rows, D, o, dtype == FA_DTYPE_BF16, lse, info->num_sms,
                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_forward_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                               int N, int D, float scale, int causal, int dtype, int num_splits, void* stream) {
+  using namespace fa;
+  if (num_splits < 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || B < 1 || H < 1 || N < 1)
+    return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (num_splits > 1 && workspace_bytes(BH, N, D, num_splits) > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
+  // The scratch address, once per device (with that device current).
+  static std::atomic<void*> scratch[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  void* ptr = scratch[dev].load(std::memory_order_acquire);
+  if (ptr == nullptr) {
+    DeviceInfo* info = nullptr;
+    const int rc = device_setup(dev, info);
+    if (rc != FA_OK) return rc;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    ptr = scratch[dev].load(std::memory_order_relaxed);
+    if (ptr == nullptr) {
+      e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_scratch);
+      if (e != cudaSuccess) return cuda_fail(e);
+      scratch[dev].store(ptr, std::memory_order_release);
+    }
+  }
+  int splits = num_splits;
+  if (splits == 0) {
+    splits = fa_splitkv_num_splits(B, H, N, D, causal);
+    if (splits < 0) return splits;
+    if (splits > 1 && workspace_bytes(BH, N, D, splits) > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
+  }
+  return forward_impl(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, splits, ptr, kNoAllocScratchBytes, stream);
 }
 
 }  // extern "C"

@@ -26,6 +26,8 @@ FA_ERR_CUDA = -4
 FA_ERR_TIMEOUT = -5
 FA_ERR_TOO_LARGE = -6
 FA_ERR_WORKSPACE = -7
+FA_ERR_SCRATCH = -8
+NOALLOC_SCRATCH_BYTES = 32 << 20
 FA_DECOMP_AUTO = 0
 FA_DECOMP_TWO_TILES = 1
 FA_DECOMP_SPLIT_KV = 2
@@ -46,6 +48,10 @@ SIGNATURES = {
                                           ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                           ctypes.c_size_t, ctypes.c_void_p]),
+    "fa_forward_splitkv_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_void_p]),
     "fa_splitkv_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_int]),
     "fa_splitkv_num_splits": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
@@ -261,5 +267,29 @@ def merge_partials(o_parts, lse_parts, out_dtype=None, out=None, lse=None):
             o_parts.data_ptr(), lse_parts.data_ptr(), P, kinds[o_parts.dtype], out.data_ptr(), lse.data_ptr(),
             B, H, N, D, FA_DTYPE_BF16 if out.dtype == torch.bfloat16 else FA_DTYPE_FP16,
             _current_stream_handle(torch, dev) or None)
+    _check(rc)
+    return out, lse
+
+
+def forward_splitkv_noalloc(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int = 0,
+                            out=None, lse=None, return_lse: bool = True):
+    """``fa_forward_splitkv_noalloc``: split-KV forward whose partials go to the library's built-in
+    32 MiB per-device scratch (no workspace argument, no allocation in the library). Calls that
+    overlap in time on one device race on that scratch."""
+    import torch
+
+    _check_qkv(torch, q, k, v)
+    B, H, N, D = q.shape
+    dev = q.get_device()
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    dtype = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
+    sc = -1.0 if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_forward_splitkv_noalloc(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            B, H, N, D, sc, 1 if causal else 0, dtype, int(num_splits), _current_stream_handle(torch, dev) or None)
     _check(rc)
     return out, lse
