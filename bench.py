@@ -259,11 +259,12 @@ def run_fa(args, w):
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     copies_used = {}
 
-    def measure(wl, steps, warmup, splits=None):
+    def measure(wl, steps, warmup, splits=None, naive=False):
         """Mean step time (ms) with the inputs cycled over enough copies to defeat L2.
 
         splits: None times fa_forward; an integer times fa_forward_splitkv with that many
-        splits (one workspace, reused by every step in stream order)."""
+        splits (one workspace, reused by every step in stream order). naive: times the
+        unfused baseline fa_naive_forward (its S/P workspace reused likewise)."""
         q0, k0, v0 = workloads.make_qkv(wl)
         set_bytes = 4 * q0.numel() * q0.element_size() + wl.B * wl.H * wl.N * 4
         n = n_copies(set_bytes)
@@ -277,10 +278,14 @@ def run_fa(args, w):
         if splits is not None:
             ws = torch.empty(max(1, fa.splitkv_workspace_bytes(wl.B, wl.H, wl.N, wl.D, splits)), dtype=torch.uint8,
                              device=dev)
+        if naive:
+            ws = torch.empty(fa.naive_workspace_bytes(wl.B, wl.H, wl.N), dtype=torch.uint8, device=dev)
 
         def fwd(i):
             q, k, v, o, lse = sets[i % n]
-            if splits is None:
+            if naive:
+                fa.naive_forward(q, k, v, causal=wl.causal, scale=wl.scale, workspace=ws, out=o, lse=lse)
+            elif splits is None:
                 fa.forward(q, k, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse)
             else:
                 fa.forward_splitkv(q, k, v, causal=wl.causal, scale=wl.scale, num_splits=splits, workspace=ws,
@@ -347,6 +352,11 @@ def run_fa(args, w):
                            "dram_bytes": tr["dram_bytes"] if tr else None,
                            "dram_vs_min": (tr["dram_bytes"] / workloads.min_dram_bytes(wl.B, wl.H, wl.N, wl.D, with_lse=False))
                            if tr else None}
+            # the unfused baseline (S and P in memory) on the fp16 workloads whose S fits in 1 GiB
+            if wl.dtype == "fp16" and wl.B * wl.H * wl.N * wl.N * 2 <= (1 << 30):
+                m3, _ = measure(wl, st, 3, naive=True)
+                sweep[name]["naive"] = {"ms_mean": m3, "tflops": f / (m3 * 1e-3) / 1e12, "fused_speedup": m3 / m,
+                                        "s_bytes": wl.B * wl.H * wl.N * wl.N * 2}
             # split-KV forward where its automatic split count is above one
             S = fa.splitkv_num_splits(wl.B, wl.H, wl.N, wl.D, wl.causal)
             if S > 1:

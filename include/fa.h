@@ -49,7 +49,8 @@ enum fa_status {
   FA_ERR_TIMEOUT = -5,     /* a device-side wait exceeded the watchdog limit */
   FA_ERR_TOO_LARGE = -6,   /* sizes exceed the 32-bit index ranges the kernel uses */
   FA_ERR_WORKSPACE = -7,   /* split-KV workspace missing, misaligned or too small */
-  FA_ERR_SCRATCH = -8      /* split-KV partials larger than the built-in scratch (noalloc) */
+  FA_ERR_SCRATCH = -8,     /* split-KV partials larger than the built-in scratch (noalloc) */
+  FA_ERR_LIBRARY = -9      /* naive baseline: cuBLAS could not be loaded or failed */
 };
 
 /*
@@ -171,6 +172,36 @@ FA_API int fa_splitkv_num_splits(int B, int H, int N, int D, int causal);
  */
 FA_API int fa_merge_partials(const void* o_parts, const float* lse_parts, int num_parts, int parts_dtype, void* o,
                              float* lse, int B, int H, int N, int D, int dtype, void* stream);
+
+/*
+ * fa_naive_forward — the unfused baseline: the same O and LSE computed the way the pages'
+ * "naive" attention does it ("Android Transformer Optimization: Attention and Mobile GPU
+ * Bottlenecks", section "The Self-Attention Bottleneck Is Memory Traffic, Not Compute"), with
+ * the whole score matrix in memory: S = scale Q K^T by a batched library GEMM (cuBLAS, the
+ * scale as alpha, as the SGEMM of "Flash Attention on Android: tiled SGEMM with
+ * RenderScript"), a row softmax kernel that writes P over S (and LSE), and O = P V by a second
+ * batched GEMM. It exists to measure what the fused kernel saves; it is not a fast path.
+ *
+ *   arguments  as fa_forward; dtype must be FA_DTYPE_FP16 (S and P are stored in fp16, as
+ *              in the pages' size claims).
+ *   workspace  caller-owned device memory of at least fa_naive_workspace_bytes(B, H, N) bytes
+ *              (S and then P, [B*H, N, N] fp16), 256-byte aligned, not overlapping any other
+ *              argument; its contents on entry do not matter.
+ *
+ * cuBLAS (libcublas.so.13) is loaded on first use; FA_ERR_LIBRARY if it cannot be loaded or
+ * a GEMM fails (fa_naive_last_library_error gives the cublasStatus_t). The first call on each
+ * host thread creates a cuBLAS handle (which allocates). Enqueues three kernels or more (the
+ * library picks its GEMM kernels) on `stream`.
+ */
+FA_API int fa_naive_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                            int D, float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* Bytes of S/P the naive baseline needs: 2 * B * H * N * N rounded up to 256; 0 if invalid. */
+FA_API size_t fa_naive_workspace_bytes(int B, int H, int N);
+
+/* The cublasStatus_t behind the most recent FA_ERR_LIBRARY on this host thread. */
+FA_API int fa_naive_last_library_error(void);
 
 /* Static description of a return code. Never NULL. */
 FA_API const char* fa_error_string(int code);

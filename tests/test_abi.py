@@ -173,3 +173,24 @@ def test_merge_rejects_bad_arguments_before_any_cuda_call(lib):
     assert _merge(lib, lp=(1 << 41) + 2) == fa.FA_ERR_ALIGN
     assert _merge(lib, o=(1 << 40) + 256) == fa.FA_ERR_INVALID_ARG         # output inside the parts
     assert _merge(lib, lse=(1 << 41) + 4) == fa.FA_ERR_INVALID_ARG         # lse inside the part lse
+
+
+def test_naive_workspace_bytes(lib):
+    assert lib.fa_naive_workspace_bytes(1, 32, 1024) == 32 * 1024 * 1024 * 2
+    assert lib.fa_naive_workspace_bytes(2, 3, 17) == _align_up(2 * 3 * 17 * 17 * 2)
+    assert lib.fa_naive_workspace_bytes(0, 1, 8) == 0
+
+
+def test_naive_rejects_bad_arguments_before_any_cuda_call(lib):
+    def call(q=16, dtype=0, D=64, ws=1 << 44, ws_bytes=1 << 30):
+        return lib.fa_naive_forward(q or None, 32, 48, 1 << 40, None, 1, 1, 256, D, 0.1, 0, dtype, ws or None,
+                                    ws_bytes, None)
+    assert call(q=0) == fa.FA_ERR_INVALID_ARG
+    assert call(dtype=1) == fa.FA_ERR_UNSUPPORTED        # the naive baseline is fp16 only
+    assert call(D=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(q=24) == fa.FA_ERR_ALIGN
+    assert call(ws=0) == fa.FA_ERR_WORKSPACE
+    assert call(ws_bytes=256 * 256 * 2 - 1) == fa.FA_ERR_WORKSPACE
+    assert call(ws=1 << 40) == fa.FA_ERR_INVALID_ARG       # workspace overlaps o
+    for code in (-8, -9):
+        assert lib.fa_error_string(code).decode() != "unknown error code"

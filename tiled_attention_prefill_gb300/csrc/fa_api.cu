@@ -432,6 +432,7 @@ const char* fa_error_string(int code) {
     case FA_ERR_TIMEOUT: return "device-side wait exceeded the watchdog limit";
     case FA_ERR_TOO_LARGE: return "sizes exceed the supported index range";
     case FA_ERR_WORKSPACE: return "split-KV workspace missing, not 256-byte aligned, or smaller than fa_splitkv_workspace_bytes";
+    case FA_ERR_LIBRARY: return "naive baseline: cuBLAS could not be loaded or a GEMM failed (see fa_naive_last_library_error)";
     case FA_ERR_SCRATCH: return "split-KV partials exceed the built-in 32 MiB scratch of fa_forward_splitkv_noalloc (use fewer splits or fa_forward_splitkv)";
     default: return "unknown error code";
   }

@@ -27,6 +27,7 @@ FA_ERR_TIMEOUT = -5
 FA_ERR_TOO_LARGE = -6
 FA_ERR_WORKSPACE = -7
 FA_ERR_SCRATCH = -8
+FA_ERR_LIBRARY = -9
 NOALLOC_SCRATCH_BYTES = 32 << 20
 FA_DECOMP_AUTO = 0
 FA_DECOMP_TWO_TILES = 1
@@ -52,6 +53,12 @@ SIGNATURES = {
                                                   ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                   ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                                   ctypes.c_int, ctypes.c_void_p]),
+    "fa_naive_forward": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                        ctypes.c_void_p]),
+    "fa_naive_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "fa_naive_last_library_error": (ctypes.c_int, []),
     "fa_splitkv_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_int]),
     "fa_splitkv_num_splits": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
@@ -291,5 +298,40 @@ def forward_splitkv_noalloc(q, k, v, causal: bool = False, scale: float | None =
         rc = load_library().fa_forward_splitkv_noalloc(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr() if lse is not None else None,
             B, H, N, D, sc, 1 if causal else 0, dtype, int(num_splits), _current_stream_handle(torch, dev) or None)
+    _check(rc)
+    return out, lse
+
+
+def naive_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(load_library().fa_naive_workspace_bytes(int(B), int(H), int(N)))
+
+
+def naive_forward(q, k, v, causal: bool = False, scale: float | None = None, workspace=None, out=None, lse=None,
+                  return_lse: bool = True):
+    """``fa_naive_forward``: the unfused baseline (S = scale QK^T and P written to memory, fp16 only).
+
+    ``workspace``: CUDA uint8 tensor of at least ``naive_workspace_bytes`` bytes (allocated here
+    when None). Returns (o, lse) like :func:`forward`.
+    """
+    import torch
+
+    _check_qkv(torch, q, k, v)
+    B, H, N, D = q.shape
+    dev = q.get_device()
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(naive_workspace_bytes(B, H, N), dtype=torch.uint8, device=q.device)
+    dtype = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
+    sc = -1.0 if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        rc = load_library().fa_naive_forward(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            B, H, N, D, sc, 1 if causal else 0, dtype, workspace.data_ptr(), workspace.numel(),
+            _current_stream_handle(torch, dev) or None)
+    if rc == FA_ERR_LIBRARY:
+        raise FAError(rc, error_string(rc) + " (cublasStatus %d)" % load_library().fa_naive_last_library_error())
     _check(rc)
     return out, lse
