@@ -257,6 +257,8 @@ def run_fa(args, w):
     stream = torch.cuda.current_stream(dev)
     peaks, peak_kind = load_peaks()
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # tf32 (the fp32-I/O kernel): the measured bf16 peak times the nominal dense ratio 1.1 / 2.25
+    peak_of = {"fp16": peak_tf, "bf16": peak_tf, "fp32": peak_tf * 1.1 / 2.25}
     copies_used = {}
 
     def measure(wl, steps, warmup, splits=None, naive=False):
@@ -348,9 +350,11 @@ def run_fa(args, w):
             m, f = measure(wl, st, 3)
             tf = f / (m * 1e-3) / 1e12
             tr = measured_traffic(name)
-            sweep[name] = {"ms_mean": m, "tflops": tf, "frac_of_peak": tf / peak_tf, "input_copies": copies_used[name][0],
+            sweep[name] = {"ms_mean": m, "tflops": tf, "frac_of_peak": tf / peak_of[wl.dtype],
+                           "peak_tflops": peak_of[wl.dtype], "input_copies": copies_used[name][0],
                            "dram_bytes": tr["dram_bytes"] if tr else None,
-                           "dram_vs_min": (tr["dram_bytes"] / workloads.min_dram_bytes(wl.B, wl.H, wl.N, wl.D, with_lse=False))
+                           "dram_vs_min": (tr["dram_bytes"] / workloads.min_dram_bytes(
+                               wl.B, wl.H, wl.N, wl.D, elem_bytes=4 if wl.dtype == "fp32" else 2, with_lse=False))
                            if tr else None}
             # the unfused baseline (S and P in memory) on the fp16 workloads whose S fits in 1 GiB
             if wl.dtype == "fp16" and wl.B * wl.H * wl.N * wl.N * 2 <= (1 << 30):

@@ -35,15 +35,18 @@
 extern "C" {
 #endif
 
-/* Element type of Q, K, V and O (fp16/bf16), and of partial outputs (also fp32).
- * Accumulation is always fp32. */
+/* Element type of Q, K, V and O, and of partial outputs. Accumulation is always fp32. For
+ * FA_DTYPE_FP32 tensors fa_forward multiplies on the tensor cores in tf32 (the fp32-storage
+ * variant of "Android Transformer Optimization: Attention and Mobile GPU Bottlenecks", section
+ * "Pitfalls I Hit"): operands read from memory keep their top 19 bits (tf32: 8-bit exponent,
+ * 10-bit mantissa), P is rounded to tf32, and the key tiles are 64 keys instead of 128. */
 enum fa_dtype { FA_DTYPE_FP16 = 0, FA_DTYPE_BF16 = 1, FA_DTYPE_FP32 = 2 };
 
 /* Return codes. */
 enum fa_status {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = -1, /* null pointer, B/H/N < 1, or O overlapping Q/K/V/LSE */
-  FA_ERR_UNSUPPORTED = -2, /* D not 64 or 128, unknown dtype, or the device is not sm_103 */
+  FA_ERR_UNSUPPORTED = -2, /* D not 64 or 128, a dtype the entry point does not take, or not sm_103 */
   FA_ERR_ALIGN = -3,       /* Q/K/V/O not 16-byte aligned, or LSE not 4-byte aligned */
   FA_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed; see fa_last_cuda_error() */
   FA_ERR_TIMEOUT = -5,     /* a device-side wait exceeded the watchdog limit */
@@ -66,7 +69,7 @@ enum fa_status {
  *   D        64 or 128.
  *   scale    multiplies q.k before the softmax; scale <= 0, NaN or Inf selects 1/sqrt(D).
  *   causal   0: every query sees every key; nonzero: query i sees keys 0..i.
- *   dtype    FA_DTYPE_FP16 or FA_DTYPE_BF16.
+ *   dtype    FA_DTYPE_FP16, FA_DTYPE_BF16, or FA_DTYPE_FP32 (tf32 tensor-core products).
  *   stream   a cudaStream_t (NULL = the legacy default stream) of the current device.
  *
  * Ownership: the caller owns every buffer; the call allocates no device memory. It is
@@ -93,7 +96,8 @@ FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, floa
  *
  * where a set with no key (lse_s = -inf) has weight 0 and its O_s is never read.
  *
- * fa_forward_splitkv computes the same O and LSE as fa_forward (arguments as there), but
+ * fa_forward_splitkv computes the same O and LSE as fa_forward (arguments as there; dtype
+ * FA_DTYPE_FP16 or FA_DTYPE_BF16 only), but
  * divides the 128-key tiles of every 128-row query tile into num_splits contiguous ranges
  * and processes each range as its own work item, so that one query tile can occupy several
  * SMs. That shortens the longest work items (the last query tiles of a causal sequence) and

@@ -71,9 +71,17 @@ def test_unsupported_head_dim(lib, D):
     assert _call(lib, D=D) == fa.FA_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("dtype", [-1, 2, 7])
+@pytest.mark.parametrize("dtype", [-1, 3, 7])
 def test_unsupported_dtype(lib, dtype):
     assert _call(lib, dtype=dtype) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_fp32_dtype_is_validated_like_the_others(lib):
+    # FA_DTYPE_FP32 is a fused-forward dtype (tf32 products): it passes validation and would
+    # then need a device; bad arguments are still refused first.
+    assert _call(lib, dtype=fa.FA_DTYPE_FP32, q=0) == fa.FA_ERR_INVALID_ARG
+    assert _call(lib, dtype=fa.FA_DTYPE_FP32, q=24) == fa.FA_ERR_ALIGN
+    assert _call(lib, dtype=fa.FA_DTYPE_FP32, D=96) == fa.FA_ERR_UNSUPPORTED
 
 
 def test_misaligned_pointers(lib):

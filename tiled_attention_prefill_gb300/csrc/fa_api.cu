@@ -14,6 +14,7 @@
 
 #include "fa.h"
 #include "fa_launch.cuh"
+#include "fa_kernel_f32.cuh"
 #include "fa_merge.cuh"
 
 namespace fa {
@@ -112,15 +113,18 @@ int device_setup(int dev, DeviceInfo*& out) {
   return d.status;
 }
 
-// [BH, N, D] 16-bit tensor viewed as 3-D (D, N, BH); box (64, box_rows, 1), 128-byte swizzle,
-// zero fill outside the tensor.
-int encode_map(CUtensorMap* map, const void* base, bool bf16, int BH, int N, int D, int box_rows) {
+// [BH, N, D] tensor viewed as 3-D (D, N, BH); box (128 bytes of columns, box_rows, 1), 128-byte
+// swizzle, zero fill outside the tensor. dtype: FA_DTYPE_FP16, _BF16 or _FP32.
+int encode_map(CUtensorMap* map, const void* base, int dtype, int BH, int N, int D, int box_rows) {
+  const cuuint64_t es = dtype == FA_DTYPE_FP32 ? 4 : 2;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * es, static_cast<cuuint64_t>(N) * D * es};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  const CUtensorMapDataType t = dtype == FA_DTYPE_FP32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                : dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = g_encode(map, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
@@ -156,6 +160,7 @@ struct LaunchEntry {
   Params params;
   int grid;
   bool splitk;
+  bool f32;        // fp32-I/O (tf32) kernel
   int splits;      // > 1: split-KV partial kernel, then the merge
   void* o;         // merge output
   float* lse;
@@ -259,7 +264,9 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+  const bool f32 = dtype == FA_DTYPE_FP32;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16 && !f32) return FA_ERR_UNSUPPORTED;
+  if (f32 && splits != 1) return FA_ERR_UNSUPPORTED;  // fp32 I/O: the fused forward only
   auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
   if (mis16(q) || mis16(k) || mis16(v) || mis16(o)) return FA_ERR_ALIGN;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
@@ -267,7 +274,7 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   const long long BH = static_cast<long long>(B) * H;
   const long long num_qt = (static_cast<long long>(N) + kBM - 1) / kBM;  // 128-row query tiles
   if (N > (1 << 30) || BH > 0x7fffffffll || BH * num_qt > 0x7fffffffll) return FA_ERR_TOO_LARGE;
-  const size_t tensor_bytes = static_cast<size_t>(BH) * N * D * 2;
+  const size_t tensor_bytes = static_cast<size_t>(BH) * N * D * (f32 ? 4 : 2);
   const size_t lse_bytes = static_cast<size_t>(BH) * N * sizeof(float);
   if (overlaps(o, tensor_bytes, q, tensor_bytes) || overlaps(o, tensor_bytes, k, tensor_bytes) ||
       overlaps(o, tensor_bytes, v, tensor_bytes) || (lse && overlaps(o, tensor_bytes, lse, lse_bytes)))
@@ -320,7 +327,9 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   for (int i = 0; i < kCacheSize; ++i) {
     const LaunchEntry& c = t_cache[i];
     if (c.valid && c.key == key) {
-      if (c.splits > 1) {
+      if (c.f32) {
+        e = launch_forward_f32(c.params, c.grid, D, key.causal != 0, s);
+      } else if (c.splits > 1) {
         e = launch_partial(c.params, c.grid, D, bf16, key.causal != 0, s);
         if (e == cudaSuccess)
           e = launch_merge(c.params.o_part, kPartsF32, c.params.lse_part, c.splits, c.rows, D, c.o, bf16, c.lse,
@@ -345,8 +354,8 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   // query tile whose K/V range is split between the two softmax warpgroups instead. The
   // split-KV partial form always uses single query tiles.
   const long long items_two = BH * ((static_cast<long long>(N) + item_rows(false) - 1) / item_rows(false));
-  bool splitk = decomp == FA_DECOMP_SPLIT_KV || splits > 1;
-  if (decomp == FA_DECOMP_AUTO && splits == 1) {
+  bool splitk = decomp == FA_DECOMP_SPLIT_KV || splits > 1 || f32;
+  if (decomp == FA_DECOMP_AUTO && splits == 1 && !f32) {
     if (causal) {
       // Unequal item costs are balanced by dispatch order; split only when the GPU is not full.
       splitk = items_two < info->num_sms;
@@ -362,10 +371,11 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   }
 
   Params p{};
-  if ((rc = encode_map(&p.tm_q, q, bf16, static_cast<int>(BH), N, D, kBM)) != FA_OK) return rc;
-  if ((rc = encode_map(&p.tm_k, k, bf16, static_cast<int>(BH), N, D, kBN)) != FA_OK) return rc;
-  if ((rc = encode_map(&p.tm_v, v, bf16, static_cast<int>(BH), N, D, kBN)) != FA_OK) return rc;
-  if ((rc = encode_map(&p.tm_o, o, bf16, static_cast<int>(BH), N, D, 32)) != FA_OK) return rc;
+  const int kv_rows = f32 ? kBNf : kBN;
+  if ((rc = encode_map(&p.tm_q, q, dtype, static_cast<int>(BH), N, D, kBM)) != FA_OK) return rc;
+  if ((rc = encode_map(&p.tm_k, k, dtype, static_cast<int>(BH), N, D, kv_rows)) != FA_OK) return rc;
+  if ((rc = encode_map(&p.tm_v, v, dtype, static_cast<int>(BH), N, D, kv_rows)) != FA_OK) return rc;
+  if ((rc = encode_map(&p.tm_o, o, dtype, static_cast<int>(BH), N, D, 32)) != FA_OK) return rc;
   p.lse = lse;
   p.status = info->status_word;
   p.timeout_ns = timeout;
@@ -374,7 +384,7 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   p.num_mb = static_cast<int>((static_cast<long long>(N) + item_rows(splitk) - 1) / item_rows(splitk));
   p.num_splits = splits;
   p.num_items = static_cast<int>(BH * p.num_mb * splits);
-  const long long kv_head_bytes = 2ll * N * D * 2;
+  const long long kv_head_bytes = 2ll * N * D * (f32 ? 4 : 2);
   long long section = kL2SectionBytes / (kv_head_bytes > 0 ? kv_head_bytes : 1);
   p.section = static_cast<int>(section < 1 ? 1 : (section > BH ? BH : section));
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
@@ -398,13 +408,16 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   slot.params = p;
   slot.grid = grid;
   slot.splitk = splitk;
+  slot.f32 = f32;
   slot.splits = splits;
   slot.o = o;
   slot.lse = lse;
   slot.rows = BH * N;
   slot.num_sms = info->num_sms;
   slot.valid = true;
-  if (splits > 1) {
+  if (f32) {
+    e = launch_forward_f32(p, grid, D, causal != 0, s);
+  } else if (splits > 1) {
     e = launch_partial(p, grid, D, bf16, causal != 0, s);
     if (e == cudaSuccess)
       e = launch_merge(p.o_part, kPartsF32, p.lse_part, splits, BH * N, D, o, bf16, lse, info->num_sms, s);

@@ -49,6 +49,9 @@ cudaError_t launch_forward(const Params& p, int grid, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// fp32-I/O (tf32) kernel: fa_inst_f32.cu.
+cudaError_t launch_forward_f32(const Params& p, int grid, int D, bool causal, cudaStream_t stream);
+
 #define FA_DECLARE_LAUNCH(EXT, D, BF16, CAUSAL)                                                              \
   EXT template cudaError_t launch_forward<D, BF16, CAUSAL, false, false>(const Params&, int, cudaStream_t); \
   EXT template cudaError_t launch_forward<D, BF16, CAUSAL, true, false>(const Params&, int, cudaStream_t);

@@ -143,7 +143,8 @@ def _current_stream_handle(torch, index: int) -> int:
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, return_lse: bool = True):
-    """Attention forward on CUDA tensors [B, H, N, D] (fp16 or bf16, contiguous).
+    """Attention forward on CUDA tensors [B, H, N, D] (fp16, bf16, or fp32 computed on tf32
+    tensor cores; contiguous).
 
     Returns (o, lse) with o like q and lse [B, H, N] fp32 (lse is None when
     ``return_lse`` is False and no buffer was given). Runs on the current stream.
@@ -152,8 +153,8 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
 
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise ValueError("q, k, v must be CUDA tensors")
-    if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise ValueError("q, k, v must share dtype fp16 or bf16")
+    if q.dtype not in (torch.float16, torch.bfloat16, torch.float32) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share dtype fp16, bf16 or fp32")
     if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must have the same shape [B, H, N, D]")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
@@ -171,7 +172,7 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     if lse is not None and (lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous()
                             or lse.get_device() != dev):
         raise ValueError("lse must be a contiguous fp32 tensor [B, H, N]")
-    dtype = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
+    dtype = {torch.float16: FA_DTYPE_FP16, torch.bfloat16: FA_DTYPE_BF16, torch.float32: FA_DTYPE_FP32}[q.dtype]
     sc = -1.0 if scale is None else float(scale)
     lib = _lib if _lib is not None else load_library()
     lse_ptr = lse.data_ptr() if lse is not None else None

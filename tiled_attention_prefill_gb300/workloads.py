@@ -20,11 +20,14 @@ discusses sequence length n=2048 in fp16, and the 32-head, D=128 setting of
   p2s512    B=1 H=32 N=512   D=128 fp16  non-causal  Q,K,V ~ N(0,1)
   p2s1024   B=1 H=32 N=1024  D=128 fp16  non-causal  Q,K,V ~ N(0,1)
   lc1       B=1 H=1  N=16384 D=128 fp16  causal      Q,K,V ~ N(0,1)
+  c2_f32    c2 in fp32 storage;  c3_f32   c3 in fp32 storage (same seeds, draws not rounded)
 
 The last two are the second workload shape of "Flash Attention on Android: tiled SGEMM
 with RenderScript" (section "Benchmark results": 32-head attention at head dim 128,
 sequence 512 and 1024); that page measured FP32, this library computes in fp16/bf16.
-``lc1`` is one long causal sequence with a single head: 128 query tiles, fewer than the
+``c2_f32`` and ``c3_f32`` are the first page's fp32-storage variant (section "Pitfalls I
+Hit": an fp32 build beside the fp16 one) on the headline and n=2048 shapes; the fp32 draws are
+used as they are. ``lc1`` is one long causal sequence with a single head: 128 query tiles, fewer than the
 GPU's SMs, the longest of them 128 key tiles long. It is the case the split-KV forward
 (partial results over key ranges, merged with the online-softmax update of the first
 page's section "The Essence of FlashAttention: Reordering the Computation") is for.
@@ -52,7 +55,7 @@ class Workload:
     H: int
     N: int
     D: int
-    dtype: str  # "fp16" | "bf16"
+    dtype: str  # "fp16" | "bf16" | "fp32"
     causal: bool
     seed: int
     qk_mult: float = 1.0
@@ -64,7 +67,7 @@ class Workload:
 
     @property
     def torch_dtype(self) -> torch.dtype:
-        return {"fp16": torch.float16, "bf16": torch.bfloat16}[self.dtype]
+        return {"fp16": torch.float16, "bf16": torch.bfloat16, "fp32": torch.float32}[self.dtype]
 
     @property
     def scale(self) -> float:
@@ -90,6 +93,10 @@ WORKLOADS = {
                         note="7B-class shape: 32 heads, N=1024, D=128, fp16, non-causal"),
     "lc1": Workload("lc1", 1, 1, 16384, 128, "fp16", True, 1008,
                     note="one long causal sequence: 1 head, N=16384, D=128, fp16"),
+    "c2_f32": Workload("c2_f32", 1, 32, 1024, 64, "fp32", True, 1002,
+                       note="c2 with fp32 storage (tf32 tensor cores): 32 heads, N=1024, D=64, causal"),
+    "c3_f32": Workload("c3_f32", 1, 32, 2048, 64, "fp32", False, 1003,
+                       note="n=2048 case with fp32 storage (tf32 tensor cores): 32 heads, D=64, non-causal"),
 }
 
 
