@@ -12,7 +12,8 @@ between two CUDA events.
 
 --impl reference times the fp64 CPU oracle on the host cores instead (a
 bounded sample of the same workload per step). --kernel-only runs just the
-warm-up and timed kernel steps (the form used under ncu).
+warm-up and timed kernel steps (the form used under ncu); with --path splitkv
+or naive it runs the split-KV forward or the unfused baseline instead.
 
 Under torchrun each rank runs its own replica of the workload (the forward
 pass has no exchange step); value = all ranks' FLOPs / the slowest rank's time.
@@ -39,7 +40,8 @@ HEADLINE = "c2"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 126 << 20
 KERNEL_SOURCES = ["tiled_attention_prefill_gb300/csrc/" + f for f in
-                  ("fa_kernel.cuh", "ptx.cuh", "fa_launch.cuh", "fa_api.cu")]
+                  ("fa_kernel.cuh", "fa_kernel_f32.cuh", "ptx.cuh", "fa_launch.cuh", "fa_api.cu", "fa_merge.cu",
+                   "fa_naive.cu", "fa_inst_f32.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_dram_traffic.json")
 
 
@@ -314,7 +316,12 @@ def run_fa(args, w):
     sampler = ClockSampler(local) if not args.kernel_only else None
     if sampler:
         sampler.start()
-    ms_local, flops = measure(w, args.steps, args.warmup)
+    if args.kernel_only and args.path != "fused":
+        # the split-KV (automatic split count) or the naive path alone, for ncu captures
+        splits = fa.splitkv_num_splits(w.B, w.H, w.N, w.D, w.causal) if args.path == "splitkv" else None
+        ms_local, flops = measure(w, args.steps, args.warmup, splits=splits, naive=args.path == "naive")
+    else:
+        ms_local, flops = measure(w, args.steps, args.warmup)
     ms = max_over_ranks(ms_local)
     value = world * flops / (ms * 1e-3) / 1e12
     if args.kernel_only:
@@ -418,6 +425,8 @@ def main():
     ap.add_argument("--impl", choices=["fa", "reference"], default="fa")
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--kernel-only", action="store_true")
+    ap.add_argument("--path", choices=["fused", "splitkv", "naive"], default="fused",
+                    help="with --kernel-only: which forward to run")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
