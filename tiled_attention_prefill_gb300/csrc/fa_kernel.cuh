@@ -17,8 +17,9 @@
 //       warp  8     tcgen05 MMA issuer (warp-uniform, one elected lane issues) and TMEM owner
 //       warp  9     TMA producer (one thread)
 //       warps 10-11 idle
-//     setmaxnreg moves registers from the third warpgroup (88 each) to the softmax
-//     warpgroups (208 each); 88 + 2 * 208 = 3 * 168, the launch allocation.
+//     At D = 128, setmaxnreg moves registers from the third warpgroup (88 each) to the softmax
+//     warpgroups (208 each); 88 + 2 * 208 = 3 * 168, the launch allocation. At D = 64 every
+//     role fits in the launch allocation and no split is made.
 //   * K and V tiles (128 keys x D) stream through a shared-memory ring filled by TMA
 //     (128-byte swizzle) in exactly the order the MMA warp consumes them.
 //   * S = Q K^T for a warpgroup goes to its own 128 TMEM columns (fp32). The warpgroup reads
@@ -59,6 +60,10 @@ constexpr int kLaunchRegs = 168;   // registers per thread at launch (65536 / 38
 constexpr int kSoftmaxRegs = 208;  // after setmaxnreg, softmax warpgroups
 constexpr int kOtherRegs = 88;     // after setmaxnreg, MMA / TMA / idle warpgroup
 static_assert(kOtherRegs + 2 * kSoftmaxRegs <= 3 * kLaunchRegs, "register split exceeds the launch pool");
+// The split is used at D = 128 only: at D = 64 every role fits the launch allocation without
+// spilling, and the 88-register MMA / TMA region would spill (measured 3-4% slower).
+template <int D>
+constexpr bool reg_split() { return D == 128; }
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kTmemCols = 512;
@@ -264,6 +269,7 @@ __device__ __forceinline__ int item_of(int k, int num_items) {
 template <int D, bool BF16, bool CAUSAL, bool SPLITK, bool PARTIAL>
 __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   static_assert(!PARTIAL || SPLITK, "the split-KV partial form uses one query tile per item");
+  constexpr bool kRegSplit = reg_split<D>();
   using L = SmemLayout<D>;
   using TC = TmemCols<D>;
   constexpr bool kSepP = TC::kSepP;
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
   grid_dependency_wait();
 
   if (warp >= 8) {
-    regs_lower<kOtherRegs>();
+    if constexpr (kRegSplit) regs_lower<kOtherRegs>();
     if (warp == kLoadWarp) {
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
@@ -604,7 +610,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
       __syncwarp();
     }  // warps 10-11: idle
   } else {
-    regs_raise<kSoftmaxRegs>();
+    if constexpr (kRegSplit) regs_raise<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax warpgroups
     const int wg = warp >> 2;        // warpgroup: query tile (two-tile items) or K parity (split-K)
     const int wq = warp & 3;         // TMEM lane quarter accessible to this warp

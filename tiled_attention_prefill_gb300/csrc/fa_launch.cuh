@@ -26,7 +26,8 @@ cudaError_t launch_forward(const Params& p, int grid, cudaStream_t stream) {
     cudaFuncAttributes attr{};
     e = cudaFuncGetAttributes(&attr, kernel);
     if (e != cudaSuccess) return e;
-    if (attr.numRegs * kNumThreads < 128 * (kOtherRegs + 2 * kSoftmaxRegs)) return cudaErrorInvalidConfiguration;
+    if (reg_split<D>() && attr.numRegs * kNumThreads < 128 * (kOtherRegs + 2 * kSoftmaxRegs))
+      return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamicBytes);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
