@@ -330,25 +330,30 @@ def run_fa(args, w):
                               "config": workload_desc(w), "kernel_only": True}), flush=True)
         return 0
 
-    # end to end through the public API: pinned host inputs -> device -> forward -> host
-    q_h, k_h, v_h = (x.pin_memory() for x in workloads.make_qkv(w))
-    q_d, k_d, v_d = (torch.empty_like(x, device=dev) for x in (q_h, k_h, v_h))
-    o_d = torch.empty_like(q_d)
-    l_d = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
-    o_h = torch.empty_like(q_h).pin_memory()
-    l_h = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    # end to end through the public API: pinned host inputs -> device -> forward -> host. q, k, v
+    # share one pinned buffer and o, lse another, so a step is one H2D copy, the forward and one
+    # D2H copy.
+    q_c, k_c, v_c = workloads.make_qkv(w)
+    numel = q_c.numel()
+    in_h = torch.empty(3 * numel, dtype=q_c.dtype).pin_memory()
+    in_h.view(3, -1).copy_(torch.stack([q_c.reshape(-1), k_c.reshape(-1), v_c.reshape(-1)]))
+    in_d = torch.empty_like(in_h, device=dev)
+    q_d, k_d, v_d = (x.view(q_c.shape) for x in in_d.view(3, -1).unbind(0))
+    o_bytes = numel * q_c.element_size()
+    l_bytes = w.B * w.H * w.N * 4
+    out_d = torch.empty(o_bytes + l_bytes, dtype=torch.uint8, device=dev)
+    out_h = torch.empty(o_bytes + l_bytes, dtype=torch.uint8).pin_memory()
+    o_d = out_d[:o_bytes].view(q_c.dtype).view(q_c.shape)
+    l_d = out_d[o_bytes:].view(torch.float32).view(w.B, w.H, w.N)
 
     def e2e_step(i):
-        q_d.copy_(q_h, non_blocking=True)
-        k_d.copy_(k_h, non_blocking=True)
-        v_d.copy_(v_h, non_blocking=True)
+        in_d.copy_(in_h, non_blocking=True)
         fa.forward(q_d, k_d, v_d, causal=w.causal, scale=w.scale, out=o_d, lse=l_d)
-        o_h.copy_(o_d, non_blocking=True)
-        l_h.copy_(l_d, non_blocking=True)
+        out_h.copy_(out_d, non_blocking=True)
 
     e2e_ms = max_over_ranks(time_steps(e2e_step, args.steps, args.warmup, stream))
-    h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h))
-    d2h = o_h.numel() * o_h.element_size() + l_h.numel() * l_h.element_size()
+    h2d = in_h.numel() * in_h.element_size()
+    d2h = out_h.numel()
 
     sweep = {}
     if not args.no_sweep:
