@@ -14,9 +14,11 @@
 //   * One CTA per SM, 384 threads = 3 warpgroups:
 //       warps 0-3   softmax warpgroup 0 (one thread per query row, TMEM lane = row)
 //       warps 4-7   softmax warpgroup 1
-//       warp  8     tcgen05 MMA issuer (warp-uniform, one elected lane issues) and TMEM owner
+//       warp  8     tcgen05 MMA issuer (warp-uniform, one elected lane issues) and TMEM owner;
+//                   at D = 64 with two query tiles per item it issues for warpgroup 0 only
 //       warp  9     TMA producer (one thread)
-//       warps 10-11 idle
+//       warp 10     at D = 64 with two query tiles per item: MMA issuer for warpgroup 1
+//       warps 10-11 otherwise idle
 //     At D = 128, setmaxnreg moves registers from the third warpgroup (88 each) to the softmax
 //     warpgroups (208 each); 88 + 2 * 208 = 3 * 168, the launch allocation. At D = 64 every
 //     role fits in the launch allocation and no split is made.
@@ -61,11 +63,12 @@ constexpr int kSoftmaxRegs = 208;  // after setmaxnreg, softmax warpgroups
 constexpr int kOtherRegs = 88;     // after setmaxnreg, MMA / TMA / idle warpgroup
 static_assert(kOtherRegs + 2 * kSoftmaxRegs <= 3 * kLaunchRegs, "register split exceeds the launch pool");
 // The split is used at D = 128 only: at D = 64 every role fits the launch allocation without
-// spilling, and the 88-register MMA / TMA region would spill (measured 3-4% slower).
+// spilling, and the smaller MMA / TMA region would spill (measured 3-4% slower).
 template <int D>
 constexpr bool reg_split() { return D == 128; }
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
+constexpr int kMmaWarp = 8;    // MMA issuer of softmax warpgroup 0, TMEM owner
+constexpr int kLoadWarp = 9;   // TMA producer
+constexpr int kMmaWarp1 = 10;  // MMA issuer of softmax warpgroup 1
 constexpr int kTmemCols = 512;
 
 // TMEM columns (fp32 S and O, packed 16-bit P). D = 128: S0 [0,128) S1 [128,256)
@@ -140,8 +143,8 @@ struct SmemLayout {
   static constexpr int kStats = kPVDone + 2;         // split-K: warpgroup 1 published (m, l)
   static constexpr int kO1Free = kStats + 1;         // split-K: warpgroup 0 finished reading O1
   static constexpr int kStall = kO1Free + 1;         // never arrived on (watchdog test hook)
-  static constexpr int kDrain = kStall + 1;
-  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kDrain = kStall + 1;          // [2] per MMA warp
+  static constexpr int kNumBars = kDrain + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kDynamicBytes = kBytes + 1024;  // slack to align the base to 1024 bytes
@@ -270,6 +273,11 @@ template <int D, bool BF16, bool CAUSAL, bool SPLITK, bool PARTIAL>
 __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   static_assert(!PARTIAL || SPLITK, "the split-KV partial form uses one query tile per item");
   constexpr bool kRegSplit = reg_split<D>();
+  // Two MMA issuers (one per softmax warpgroup) where that measured faster: D = 64 with two
+  // query tiles per item (c3 43.2 -> 40.5 us). At D = 128 and with single query tiles one
+  // issuer is faster (two made c4 8%, c5 10% and the short causal c2 7% slower).
+  constexpr bool kDualMma = (D == 64) && !SPLITK;
+  constexpr uint32_t kMmaIssuers = kDualMma ? 2 : 1;
   using L = SmemLayout<D>;
   using TC = TmemCols<D>;
   constexpr bool kSepP = TC::kSepP;
@@ -293,10 +301,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::kQFull), 1);
-    mbar_init(bar(L::kQEmpty), 1);
+    mbar_init(bar(L::kQEmpty), kMmaIssuers);  // one arrival per MMA warp
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::kKVFull + s), 1);
-      mbar_init(bar(L::kKVEmpty + s), 1);
+      mbar_init(bar(L::kKVEmpty + s), kMmaIssuers);  // one release per MMA warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(L::kSFull + i), 1);
@@ -309,6 +317,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
     mbar_init(bar(L::kO1Free), kBM);
     mbar_init(bar(L::kStall), 1);
     mbar_init(bar(L::kDrain), 1);
+    mbar_init(bar(L::kDrain + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -397,8 +406,170 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
         }
       }
       __syncwarp();
-    } else if (warp == kMmaWarp) {
-      // ------------------------------------------------------------ MMA issuer
+    } else if (kDualMma && (warp == kMmaWarp || warp == kMmaWarp1)) {
+      // ------------------------------------------------------------ MMA issuers (dual, D = 64, two query tiles)
+      // Warp kMmaWarp issues every MMA of softmax warpgroup 0 (its S and its PV), warp
+      // kMmaWarp1 those of warpgroup 1. Issuing a tcgen05.mma blocks the warp for about the
+      // MMA's tensor time, so one issuer would leave the tensor pipe idle whenever it waited
+      // for one warpgroup; with one issuer per warpgroup, the other one keeps the pipe fed.
+      // Both walk every K/V ring position in the producer's order (waiting for each one, so no
+      // phase can be mistaken for a later one) and release every position: with a commit where
+      // they used it, with a plain arrive where the tile belongs to the other warpgroup. A stage
+      // is free once both released it. The whole warp runs the loop; one elected lane issues.
+      {
+        const int w = warp == kMmaWarp ? 0 : 1;  // the warpgroup this warp serves
+        const uint32_t leader = elect_one_lane();
+        constexpr uint32_t idesc_s = instr_desc_f16(BF16, kBM, kBN, false);
+        constexpr uint32_t idesc_o = instr_desc_f16(BF16, kBM, D, true);
+        uint32_t kv_pos = 0, items = 0, merges = 0, pcnt = 0, tiles_w = 0;
+        bool ok = true;
+        auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
+          return __all_sync(0xffffffffu, wait_phase(b, parity, watch, site));
+        };
+        // Next K/V ring slot: wait until TMA has filled it; returns its stage.
+        auto next_slot = [&](uint32_t& stage) -> bool {
+          stage = kv_pos % L::kStages;
+          if (!wait(bar(L::kKVFull + stage), (kv_pos / L::kStages) & 1, 3)) return false;
+          ++kv_pos;
+          tc_fence_after();
+          return true;
+        };
+        auto release = [&](uint32_t stage) { mma_commit_leader(bar(L::kKVEmpty + stage), leader); };
+        auto pass = [&](uint32_t stage) {  // a position this warpgroup does not use
+          if (leader) mbar_arrive(bar(L::kKVEmpty + stage));
+        };
+
+        // Descriptors are built once; per stage / tile / k-step only the 14-bit start-address
+        // field (address >> 4, no carry possible below 256 KB) is advanced.
+        const uint64_t q_desc = smem_desc_sw128(q_addr(0), 16, 1024);
+        const uint64_t k_desc = smem_desc_sw128(kv_addr(0), 16, 1024);
+        const uint64_t v_desc = smem_desc_sw128(kv_addr(0), L::kChunkBytes, 1024);
+        constexpr uint32_t kTileEnc = L::kTileBytes >> 4;
+
+        // S_w = Q_qi K^T into TMEM columns [128 w, 128 w + 128). Q is released (one of the two
+        // arrivals kQEmpty needs) once this warpgroup's last S MMA of the item has been issued.
+        int s_left = 0;  // S MMAs of the current item not yet issued for this warpgroup
+        auto issue_s = [&](int qi, uint32_t stage) {
+          const uint32_t d_tmem = tmem + TC::s(w);
+          const uint64_t a0 = q_desc + static_cast<uint32_t>(qi) * kTileEnc;
+          const uint64_t b0 = k_desc + stage * kTileEnc;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+            mma_ss_leader(d_tmem, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u, leader);
+          }
+          mma_commit_leader(bar(L::kSFull + w), leader);
+          if (--s_left == 0) mma_commit_leader(bar(L::kQEmpty), leader);
+        };
+        // O_w (+)= P_w V; P_w is 64 columns of packed fp16/bf16 pairs (TmemCols).
+        // V tile: keys are the K dimension (rows, 128 B apart), D is the N dimension (MN-major):
+        // 8-key groups are 1024 B apart, 64-column chunks kChunkBytes apart (the LBO).
+        auto issue_pv = [&](uint32_t stage, bool accumulate, bool last) -> bool {
+          if (!wait(bar(L::kPFull + w), pcnt & 1, 5 + w)) return false;
+          ++pcnt;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + TC::o(w);
+          const uint32_t a_tmem = tmem + TC::p(w);
+          const uint64_t b0 = v_desc + stage * kTileEnc;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts_leader(d_tmem, a_tmem + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_o,
+                          (accumulate || kk > 0) ? 1u : 0u, leader);
+          if (kSepP) mma_commit_leader(bar(L::kPVDone + w), leader);
+          if (last) mma_commit_leader(bar(L::kOFull + w), leader);
+          return true;
+        };
+        // Separate-P form: the warpgroup signals kSFree once per tile it processes, so the
+        // hand-back of its tile u of the current item is completion tiles_w + u + 1.
+        auto wait_s_free = [&](int u) -> bool {
+          const uint32_t c = tiles_w + static_cast<uint32_t>(u) + 1;
+          if (!wait(bar(L::kSFree + w), (c - 1) & 1, 14 + w)) return false;
+          tc_fence_after();
+          return true;
+        };
+
+        if (p.force_stall) ok = wait(bar(L::kStall), 0, 12);  // runs out: exercises the abort path
+        for (int k = 0; ok; ++k) {
+          const int t = item_of(k, p.num_items);
+          if (t < 0) break;
+          int jb, nk, n0, n1;
+          decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, jb, nk, n0, n1);
+          if (nk == 0) continue;  // empty split-KV range
+          const int n_w = w ? n1 : n0;
+          if (!(ok = wait(bar(L::kQFull), items & 1, 2))) break;
+          s_left = n_w;
+          if (n_w == 0 && leader) mbar_arrive(bar(L::kQEmpty));  // nothing of this item to issue
+          // Key tile j is this warpgroup's u-th tile (or not its own).
+          auto own = [&](int j, int& u) -> bool {
+            if (SPLITK) {
+              u = j >> 1;
+              return (j & 1) == w;
+            }
+            u = j;
+            return j < n_w;
+          };
+          auto on_k = [&](int j) -> bool {
+            uint32_t st;
+            if (!next_slot(st)) return false;
+            int u;
+            if (!own(j, u)) {
+              pass(st);
+              return true;
+            }
+            // With separate P the next S only needs the previous S read; otherwise it follows the
+            // PV that read P (same columns) in this warp's in-order issue.
+            if (kSepP && u > 0 && !wait_s_free(u - 1)) return false;
+            issue_s(SPLITK ? 0 : w, st);
+            release(st);
+            return true;
+          };
+          auto on_v = [&](int j) -> bool {
+            uint32_t st;
+            if (!next_slot(st)) return false;
+            int u;
+            if (!own(j, u)) {
+              pass(st);
+              return true;
+            }
+            // Warpgroup 1's O is overwritten by its first PV: the previous merge must have read it.
+            if (SPLITK && w == 1 && u == 0 && merges > 0 && !wait(bar(L::kO1Free), (merges - 1) & 1, 13))
+              return false;
+            if (!issue_pv(st, u > 0, u == n_w - 1)) return false;
+            release(st);
+            return true;
+          };
+          // The producer's order (see the producer).
+          if (!SPLITK && !kSepP) {
+            for (int j = 0; j < nk && ok; ++j) ok = on_k(j) && on_v(j);
+          } else if (SPLITK && kSepP) {
+            ok = on_k(0);
+            if (ok && nk > 1) ok = on_k(1);
+            for (int t2 = 0; t2 < nk && ok; t2 += 2) {
+              if (t2 + 2 < nk) ok = on_k(t2 + 2);
+              if (ok && t2 + 3 < nk) ok = on_k(t2 + 3);
+              ok = ok && on_v(t2);
+              if (ok && t2 + 1 < nk) ok = on_v(t2 + 1);
+            }
+          } else {
+            ok = on_k(0);
+            for (int j = 0; j < nk && ok; ++j) {
+              if (j + 1 < nk) ok = on_k(j + 1);
+              ok = ok && on_v(j);
+            }
+          }
+          if (!ok) break;
+          if (SPLITK && w == 1 && n1 > 0) ++merges;
+          ++items;
+          tiles_w += static_cast<uint32_t>(n_w);
+        }
+        // Whatever happened, wait for every MMA this warp issued before TMEM can be freed.
+        mma_commit_leader(bar(L::kDrain + w), leader);
+        if (leader) wait_phase_drain(bar(L::kDrain + w), 0);
+      }
+      __syncwarp();
+    } else if (!kDualMma && warp == kMmaWarp) {
+      // ------------------------------------------------------------ MMA issuer (single)
+      // One warp issues the MMAs of both softmax warpgroups (D = 128 and single-query-tile items).
       // The whole warp runs this loop; one elected lane issues each tcgen05 instruction.
       {
         const uint32_t leader = elect_one_lane();
@@ -608,7 +779,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
         if (leader) wait_phase_drain(bar(L::kDrain), 0);
       }
       __syncwarp();
-    }  // warps 10-11: idle
+    }  // the remaining warps of this warpgroup: idle
   } else {
     if constexpr (kRegSplit) regs_raise<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax warpgroups
