@@ -39,9 +39,9 @@ UNIT = "TFLOP/s"
 HEADLINE = "c2"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 126 << 20
+# The sources of the fused kernels whose DRAM traffic profiles/fa_fwd_dram_traffic.json records.
 KERNEL_SOURCES = ["tiled_attention_prefill_gb300/csrc/" + f for f in
-                  ("fa_kernel.cuh", "fa_kernel_f32.cuh", "ptx.cuh", "fa_launch.cuh", "fa_api.cu", "fa_merge.cu",
-                   "fa_naive.cu", "fa_inst_f32.cu")]
+                  ("fa_kernel.cuh", "fa_kernel_f32.cuh", "ptx.cuh", "fa_launch.cuh", "fa_api.cu", "fa_inst_f32.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_dram_traffic.json")
 
 

@@ -76,17 +76,18 @@ __global__ void __launch_bounds__(kMergeThreads) fa_merge_kernel(const TP* __res
        row < rows; row += step) {
     float m = -INFINITY, l = 0.f;
     F4 acc{0.f, 0.f, 0.f, 0.f};
-    // Parts in groups of kGroup: the lse and O loads of a group are issued before any of them
-    // is used, so several loads per thread are in flight.
+    // Parts in groups of kGroup: the lse and O loads of a group are all issued before any of
+    // them is used (the O addresses do not depend on lse), so one memory round trip covers the
+    // group. A part whose lse is -inf is skipped below, whatever its O holds.
     for (int s0 = 0; s0 < num_parts; s0 += kGroup) {
       float ms[kGroup];
       F4 v[kGroup];
 #pragma unroll
-      for (int u = 0; u < kGroup; ++u)
-        ms[u] = s0 + u < num_parts ? __ldg(lse_parts + static_cast<long long>(s0 + u) * rows + row) : -INFINITY;
-#pragma unroll
-      for (int u = 0; u < kGroup; ++u)
-        if (ms[u] > -INFINITY) v[u] = load4<TP>(o_parts + (static_cast<long long>(s0 + u) * rows + row) * D + 4 * sub);
+      for (int u = 0; u < kGroup; ++u) {
+        const bool in = s0 + u < num_parts;
+        ms[u] = in ? __ldg(lse_parts + static_cast<long long>(s0 + u) * rows + row) : -INFINITY;
+        v[u] = in ? load4<TP>(o_parts + (static_cast<long long>(s0 + u) * rows + row) * D + 4 * sub) : F4{0.f, 0.f, 0.f, 0.f};
+      }
 #pragma unroll
       for (int u = 0; u < kGroup; ++u) {
         const float m_s = ms[u];
