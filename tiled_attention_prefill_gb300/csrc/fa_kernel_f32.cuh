@@ -12,8 +12,8 @@
 //                   the item's query tile; warpgroup 0 merges both partial (m, l, O) at the end
 //   warp 8          MMA issuer (whole warp, one elected lane issues) and TMEM owner
 //   warp 9          TMA producer
-//   warps 10-11     V transposers: one thread per key row copies each V tile into a K-major
-//                   tile (Vt) for the PV product (the MMAs here read tf32 operands K-major)
+//   warps 10-11     V transposers: copy each V tile, in 4 x 4 blocks, into a K-major tile (Vt)
+//                   for the PV product (the MMAs here read tf32 operands K-major)
 // K and V tiles stream through separate rings: the MMA warp is the only reader of the K ring
 // and the transposers the only readers of the V ring, so each waits on every position of its
 // ring in order and an mbarrier phase can never be mistaken for one two phases later.
@@ -105,12 +105,11 @@ __device__ __forceinline__ void mma_ts_tf32_leader(uint32_t d_tmem, uint32_t a_t
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
       : "memory");
 }
-// fp32 -> tf32, round to nearest (ties away), kept in a 32-bit register.
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
+// fp32 -> tf32, rounded to nearest (ties away from zero), in a 32-bit register: half a tf32
+// unit (bit 12) is added to the fp32 bits, and the tensor core, which reads the top 19 bits of
+// a tf32 operand, drops the rest. For finite x >= 0 (every P) this gives the bits of
+// cvt.rna.tf32.f32 in one integer add; the kernel's outputs were measured bit-identical.
+__device__ __forceinline__ uint32_t to_tf32_for_mma(float x) { return __float_as_uint(x) + 0x1000u; }
 
 // Key tiles (64 keys) of the item's query tile: all of them, or causally those that hold a
 // key <= the tile's last row; warpgroup w processes tiles j = w, w + 2, ...
@@ -341,10 +340,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_f32_kernel(const __grid
       __syncwarp();
     } else {
       // ------------------------------------------------------------ V transposers (warps 10-11)
-      // Thread t owns key row t of each V tile: it reads the row (D fp32, 128-byte swizzled
-      // chunks of 32 columns) and writes element d to row d of Vt (K-major: 64 keys in two
-      // 128-byte swizzled chunks). The ring position sequence is the producer's: per item K0,
-      // V ring positions and transposed buffers are both taken in V order.
+      // Element (key, d) of a V tile (64 keys x D fp32 as loaded: 128-byte swizzled chunks of
+      // 32 columns) goes to row d of Vt (K-major: the 64 keys of a row in two 128-byte swizzled
+      // chunks). V ring positions and transposed buffers are both taken in V order.
       const int t = threadIdx.x - 320;  // 0..63
       uint32_t v_pos = 0, vt_cnt = 0;
       bool ok = true;
@@ -361,22 +359,38 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_f32_kernel(const __grid
           if (!(ok = wait_phase(bar(L::kVtEmpty + buf), ((vt_cnt / L::kNumVt) & 1) ^ 1, watch, 15))) break;
           ++v_pos;
           ++vt_cnt;
-          const uint32_t src = v_addr(stage) + t * 128;
-          const uint32_t dst = vt_addr(buf) + (t >> 5) * L::kVtChunkBytes + (t & 3) * 4;
-          const uint32_t key_unit = (t & 31) >> 2;
-#pragma unroll 4
-          for (int u = 0; u < D / 4; ++u) {  // 16-byte unit u of the row: columns 4u .. 4u + 3
-            const uint32_t c = u >> 3, uu = u & 7;
-            uint32_t x0, x1, x2, x3;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                         : "r"(src + c * L::kKVChunkBytes + ((uu ^ (t & 7)) << 4)));
-            const uint32_t xs[4] = {x0, x1, x2, x3};
+          // 4 x 4 blocks (keys 4g .. 4g + 3, columns 4uf .. 4uf + 3): four 16-byte loads of V
+          // rows, four 16-byte stores of Vt rows. The eight lanes of a quarter warp take one
+          // diagonal of an 8 x 8 grid of blocks, so each load and each store touches eight
+          // distinct 16-byte bank groups.
+          {
+            constexpr int kColChunks = D / 32;
+            constexpr int kPerQuarter = 2 * kColChunks;  // (2 key chunks x kColChunks x 8 diagonals) / 8 quarters
+            const int quarter = t >> 3, l8 = t & 7;
+            const uint32_t vsrc = v_addr(stage), vdst = vt_addr(buf);
+#pragma unroll 2
+            for (int k2 = 0; k2 < kPerQuarter; ++k2) {
+              const int idx = quarter * kPerQuarter + k2;
+              const int sft = idx & 7, C = (idx >> 3) % kColChunks, G = idx / (8 * kColChunks);
+              const int g = 8 * G + l8;
+              const int u = (l8 + sft) & 7;
+              const int uf = 8 * C + u;
+              uint32_t x[4][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t d = 4 * u + e;
-              asm volatile("st.shared.b32 [%0], %1;" ::"r"(dst + d * 128 + ((key_unit ^ (d & 7)) << 4)), "r"(xs[e])
-                           : "memory");
+              for (int i = 0; i < 4; ++i) {
+                const int r = 4 * g + i;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(x[i][0]), "=r"(x[i][1]), "=r"(x[i][2]), "=r"(x[i][3])
+                             : "r"(vsrc + C * L::kKVChunkBytes + r * 128 + ((u ^ (r & 7)) << 4)));
+              }
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int d = 4 * uf + e;
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(vdst + G * L::kVtChunkBytes + d * 128 +
+                                                                            (((g & 7) ^ (d & 7)) << 4)),
+                             "r"(x[0][e]), "r"(x[1][e]), "r"(x[2][e]), "r"(x[3][e])
+                             : "memory");
+              }
             }
           }
           fence_proxy_async_smem();  // the MMA (async proxy) reads Vt; TMA refills the V stage
@@ -453,7 +467,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_f32_kernel(const __grid
         for (int c = 0; c < kBNf; ++c) {
           const float pv = ex2_approx(fmaf(s[c], sl2, -m_base));
           acc[c & 3] += pv;
-          sr[c] = to_tf32(pv);
+          sr[c] = to_tf32_for_mma(pv);
         }
         l_run += (acc[0] + acc[1]) + (acc[2] + acc[3]);
         tmem_st32x32b_x64(t_s, sr);  // P over S
