@@ -18,11 +18,17 @@
 // and the transposers the only readers of the V ring, so each waits on every position of its
 // ring in order and an mbarrier phase can never be mistaken for one two phases later.
 // TMEM: S_w (fp32, 64 columns) at 64 w; P_w (tf32, rounded to nearest) overwrites S_w; O_w
-// (fp32, D columns) at 128 + D w. Per warpgroup the MMA order is S(j), PV(j), S(j + 2), so the
-// in-order tensor pipe keeps S(j + 2) from overwriting P(j) before PV(j) has read it.
+// (fp32, D columns) at 128 + D w; Q (D columns) after them. Per warpgroup the MMA order is
+// S(j), PV(j), S(j + 2), so the in-order tensor pipe keeps S(j + 2) from overwriting P(j)
+// before PV(j) has read it.
+//
+// Q is copied from its TMA tile into TMEM once per item (tcgen05.cp) and S = Q K^T reads it
+// there. With both operands in shared memory an S step reads 6 KB for 32 cycles of tensor
+// work; steps that read 6 KB from shared memory were measured at 48 cycles (128 bytes per
+// cycle). From TMEM only the 2 KB of K is read.
 //
 // Operand layouts (128-byte swizzle, 32 fp32 per 128-byte row segment):
-//   Q tile  128 x D, K-major A of S = Q K^T; D / 32 chunks of 128 rows x 128 bytes
+//   Q tile  128 x D, as loaded by TMA; D / 32 chunks of 128 rows x 128 bytes, copied to TMEM
 //   K tile  64 x D,  K-major B of S;           D / 32 chunks of 64 rows x 128 bytes
 //   V tile  64 x D,  as loaded (keys are rows); transposed in shared memory into
 //   Vt      D x 64,  K-major B of O += P V (D is N, keys are K); 2 chunks of D rows x 128 bytes
@@ -75,8 +81,10 @@ struct SmemLayoutF32 {
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kDynamicBytes = kBytes + 1024;
   static_assert(kDynamicBytes <= 232448, "shared memory budget");
-  static constexpr uint32_t kTmemCols = (D == 64) ? 256 : 512;
-  static_assert(2 * kBNf + 2 * D <= static_cast<int>(kTmemCols), "TMEM budget");
+  // TMEM: S_w (64 columns) at 64 w, O_w (D columns) at 128 + D w, Q (tf32, D columns) after them.
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kQCol = 2 * kBNf + 2 * D;
+  static_assert(kQCol + D <= kTmemCols, "TMEM budget");
 };
 
 // tcgen05 instruction descriptor, kind::tf32: D fp32, A and B tf32 (format 2).
@@ -85,14 +93,14 @@ __host__ __device__ constexpr uint32_t instr_desc_tf32(int M, int N, bool b_mn_m
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_ss_tf32_leader(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                   uint32_t accumulate, uint32_t leader) {
+// Copies a 128-row x 256-bit slice of a shared-memory matrix (the layout its descriptor gives)
+// into 128 TMEM lanes x 8 columns; asynchronous, ordered before later tcgen05.mma of this thread.
+__device__ __forceinline__ void tmem_cp_128x256b_leader(uint32_t taddr, uint64_t s_desc, uint32_t leader) {
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "setp.ne.b32 q, %5, 0;\n\t"
-      "@q tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %2, 0;\n\t"
+      "@q tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(s_desc), "r"(leader)
       : "memory");
 }
 __device__ __forceinline__ void mma_ts_tf32_leader(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -258,19 +266,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_f32_kernel(const __grid
       const uint64_t vt_desc = smem_desc_sw128(vt_addr(0), 16, 1024);
       constexpr uint32_t kStageEnc = L::kKVBytes >> 4;
       uint32_t vt_cnt = 0;  // V tiles consumed (transposed buffers used in turn)
-      int s_left = 0;
-      // S_w = Q K^T (64 columns at 64 w): D / 8 steps of K = 8 (32 bytes of a row segment).
+      // S_w = Q K^T (64 columns at 64 w): D / 8 steps of K = 8. A is Q in TMEM (8 columns per
+      // step), B the K tile in shared memory (32 bytes of a row segment per step).
       auto issue_s = [&](int w, uint32_t stage) {
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(w * kBNf);
         const uint64_t b0 = k_desc + stage * kStageEnc;
 #pragma unroll
         for (int kk = 0; kk < D / 8; ++kk) {
-          const uint32_t a_off = ((kk >> 2) * L::kQChunkBytes + (kk & 3) * 32) >> 4;
           const uint32_t b_off = ((kk >> 2) * L::kKVChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss_tf32_leader(d_tmem, q_desc + a_off, b0 + b_off, idesc_s, kk > 0 ? 1u : 0u, leader);
+          mma_ts_tf32_leader(d_tmem, tmem + L::kQCol + 8 * kk, b0 + b_off, idesc_s, kk > 0 ? 1u : 0u, leader);
         }
         mma_commit_leader(bar(L::kSFull + w), leader);
-        if (--s_left == 0) mma_commit_leader(bar(L::kQEmpty), leader);
       };
       // The next transposed V tile (written by the transposers, in V order).
       auto next_vt = [&](uint32_t& buf) -> bool {
@@ -307,8 +313,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_f32_kernel(const __grid
         const Item it = decode_item<CAUSAL>(t, p);
         int nk, n0, n1;
         tile_counts_f32<CAUSAL>(it.mb, p.N, nk, n0, n1);
-        s_left = nk;
         if (!(ok = wait(bar(L::kQFull), items & 1, 2))) break;
+        tc_fence_after();
+        // Q into TMEM, one 8-column step of K at a time. The copies follow the previous item's
+        // last S MMA in issue order, and the shared-memory Q tile is free for the next item's
+        // load once they complete.
+#pragma unroll
+        for (int kk = 0; kk < D / 8; ++kk)
+          tmem_cp_128x256b_leader(tmem + L::kQCol + 8 * kk,
+                                  q_desc + (((kk >> 2) * L::kQChunkBytes + (kk & 3) * 32) >> 4), leader);
+        mma_commit_leader(bar(L::kQEmpty), leader);
         uint32_t sk, sv;
         // S_0(K0), S_1(K1), then per j: PV_{j&1}(V_j), S_{j&1}(K_{j+2}).
         if (!(ok = next_k(sk))) break;
