@@ -249,6 +249,22 @@ FA_API int fa_set_decomposition(int mode);
  */
 FA_API int fa_debug_force_stall(int on);
 
+/*
+ * Inspection hook for the work schedule (host only, no CUDA call): causal problems with more
+ * than two waves of work items run on a persistent grid of num_sms CTAs whose item lists
+ * reproduce one-CTA-per-item hardware dispatch in the item order (each item goes to the CTA
+ * that frees up first under an estimated cost). This returns the lists fa_forward would use
+ * for this shape on a GPU with num_sms SMs, with the current fa_set_decomposition mode:
+ * out[0 .. num_sms] are offsets, and CTA c processes the items out[num_sms + 1 + i] for i in
+ * [out[c], out[c + 1]), in that order. Items are numbered in the kernel's order (per head
+ * section, row blocks longest first). Returns the number of ints (num_sms + 1 + items),
+ * 0 when the shape uses no schedule (the items are then strided over the CTAs), the same
+ * count without writing when out is NULL, FA_ERR_INVALID_ARG for bad sizes or when capacity
+ * is too small, FA_ERR_UNSUPPORTED for D or dtype, FA_ERR_TOO_LARGE past the item limit.
+ */
+FA_API int fa_debug_work_schedule(int B, int H, int N, int D, int causal, int dtype, int num_sms, int* out,
+                                  int capacity);
+
 /* The cudaError_t value behind the most recent FA_ERR_CUDA returned on this host thread. */
 FA_API int fa_last_cuda_error(void);
 

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <functional>
+#include <map>
 #include <mutex>
 #include <queue>
 #include <vector>
@@ -257,6 +258,124 @@ int choose_splits(long long BH, int N, int D, bool causal, int num_sms) {
   return best;
 }
 
+// Work decomposition and item order of a forward (the Params fields BH, N, num_mb, num_splits,
+// num_items, section). Two query tiles per item halve the K/V traffic per query row; when that
+// leaves too few items to fill the GPU (short or few sequences), each item is a single query
+// tile whose K/V range is split between the two softmax warpgroups instead. The split-KV
+// partial form and the fp32 kernel always use single query tiles.
+struct WorkPlan {
+  bool splitk;       // single-query-tile items
+  bool by_dispatch;  // causal with more than two waves of items: items follow dispatch order
+};
+WorkPlan plan_work(Params& p, long long BH, int N, int D, bool causal, bool f32, int splits, int decomp, int num_sms) {
+  const long long items_two = BH * ((static_cast<long long>(N) + item_rows(false) - 1) / item_rows(false));
+  bool splitk = decomp == FA_DECOMP_SPLIT_KV || splits > 1 || f32;
+  if (decomp == FA_DECOMP_AUTO && splits == 1 && !f32) {
+    if (causal) {
+      // Unequal item costs are balanced by dispatch order; split only when the GPU is not full.
+      splitk = items_two < num_sms;
+    } else {
+      // Equal item costs: compare how well each item count fills whole waves of SMs. The
+      // split-KV form pays a few percent for its extra K/V traffic and merge.
+      auto wave_eff = [&](long long n) {
+        const long long waves = (n + num_sms - 1) / num_sms;
+        return static_cast<double>(n) / static_cast<double>(waves * num_sms);
+      };
+      splitk = wave_eff(2 * items_two) * 0.96 > wave_eff(items_two);
+    }
+  }
+  p.BH = static_cast<int>(BH);
+  p.N = N;
+  p.num_mb = static_cast<int>((static_cast<long long>(N) + item_rows(splitk) - 1) / item_rows(splitk));
+  p.num_splits = splits;
+  p.num_items = static_cast<int>(BH * p.num_mb * splits);
+  const long long kv_head_bytes = 2ll * N * D * (f32 ? 4 : 2);
+  const long long section = kL2SectionBytes / (kv_head_bytes > 0 ? kv_head_bytes : 1);
+  p.section = static_cast<int>(section < 1 ? 1 : (section > BH ? BH : section));
+  return WorkPlan{splitk, causal && p.num_items > 2 * num_sms && splits == 1};
+}
+
+// Item lists for a persistent grid that follow the one-CTA-per-item dispatch: in item order
+// (decode_item), each item goes to the CTA that frees up first under an estimated cost, the
+// key tiles of its longer warpgroup chain plus a fixed per-item overhead (in tile units). The
+// persistent CTA then prefetches the next item's Q and K/V during the current one, which the
+// per-item launch cannot. Device copies live per device and shape for the process lifetime.
+struct ScheduleKey {
+  int dev, BH, N, causal, splitk, f32, section, num_mb, num_items, grid;
+  bool operator<(const ScheduleKey& o) const { return std::memcmp(this, &o, sizeof(ScheduleKey)) < 0; }
+};
+std::mutex g_schedule_mutex;
+std::map<ScheduleKey, int*> g_schedules;
+constexpr double kScheduleItemOverhead = 1.0;
+
+std::vector<int> build_schedule(const Params& p, bool causal, bool splitk, bool f32, int grid) {
+  const int n = p.num_items;
+  using Slot = std::pair<double, int>;  // (estimated time the CTA frees up, CTA)
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+  for (int c = 0; c < grid; ++c) free_at.push({0.0, c});
+  std::vector<std::vector<int>> lists(grid);
+  for (int t = 0; t < n; ++t) {
+    const Item it = causal ? decode_item<true>(t, p) : decode_item<false>(t, p);
+    int nk = 0, n0 = 0, n1 = 0;
+    if (f32) {
+      if (causal) tile_counts_f32<true>(it.mb, p.N, nk, n0, n1);
+      else tile_counts_f32<false>(it.mb, p.N, nk, n0, n1);
+    } else if (splitk) {
+      if (causal) tile_counts<true, true>(it.mb, p.N, nk, n0, n1);
+      else tile_counts<false, true>(it.mb, p.N, nk, n0, n1);
+    } else {
+      if (causal) tile_counts<true, false>(it.mb, p.N, nk, n0, n1);
+      else tile_counts<false, false>(it.mb, p.N, nk, n0, n1);
+    }
+    const Slot c = free_at.top();
+    free_at.pop();
+    lists[c.second].push_back(t);
+    free_at.push({c.first + kScheduleItemOverhead + std::max(n0, n1), c.second});
+  }
+  std::vector<int> out(static_cast<size_t>(grid) + 1 + n);
+  int off = 0;
+  for (int c = 0; c < grid; ++c) {
+    out[c] = off;
+    for (int t : lists[c]) out[grid + 1 + off++] = t;
+  }
+  out[grid] = off;
+  return out;
+}
+
+// The device copy of the schedule for this shape, made on first use (nullptr while the stream is
+// being captured into a graph or when the copy fails: the caller then launches one CTA per item).
+const int* get_schedule(int dev, const Params& p, bool causal, bool splitk, bool f32, int grid, cudaStream_t s) {
+  ScheduleKey key{};
+  key.dev = dev;
+  key.BH = p.BH;
+  key.N = p.N;
+  key.causal = causal;
+  key.splitk = splitk;
+  key.f32 = f32;
+  key.section = p.section;
+  key.num_mb = p.num_mb;
+  key.num_items = p.num_items;
+  key.grid = grid;
+  std::lock_guard<std::mutex> lock(g_schedule_mutex);
+  auto found = g_schedules.find(key);
+  if (found != g_schedules.end()) return found->second;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
+  const std::vector<int> host = build_schedule(p, causal, splitk, f32, grid);
+  int* d = nullptr;
+  if (cudaMalloc(&d, host.size() * sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cudaMemcpy(d, host.data(), host.size() * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(d);
+    return nullptr;
+  }
+  g_schedules[key] = d;
+  return d;
+}
+
 // Shared by fa_forward (splits = 1) and fa_forward_splitkv (splits >= 1 after the automatic
 // choice). Validation first, then the per-thread launch cache, then descriptor encoding.
 int forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
@@ -349,28 +468,9 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
     if (splits > 1 && (rc = check_workspace(splits)) != FA_OK) return rc;
   }
 
-  // Work decomposition. Two query tiles per item halve the K/V traffic per query row; when
-  // that leaves too few items to fill the GPU (short or few sequences), each item is a single
-  // query tile whose K/V range is split between the two softmax warpgroups instead. The
-  // split-KV partial form always uses single query tiles.
-  const long long items_two = BH * ((static_cast<long long>(N) + item_rows(false) - 1) / item_rows(false));
-  bool splitk = decomp == FA_DECOMP_SPLIT_KV || splits > 1 || f32;
-  if (decomp == FA_DECOMP_AUTO && splits == 1 && !f32) {
-    if (causal) {
-      // Unequal item costs are balanced by dispatch order; split only when the GPU is not full.
-      splitk = items_two < info->num_sms;
-    } else {
-      // Equal item costs: compare how well each item count fills whole waves of SMs. The
-      // split-KV form pays a few percent for its extra K/V traffic and merge.
-      auto wave_eff = [&](long long n) {
-        const long long waves = (n + info->num_sms - 1) / info->num_sms;
-        return static_cast<double>(n) / static_cast<double>(waves * info->num_sms);
-      };
-      splitk = wave_eff(2 * items_two) * 0.96 > wave_eff(items_two);
-    }
-  }
-
   Params p{};
+  const WorkPlan plan = plan_work(p, BH, N, D, causal != 0, f32, splits, decomp, info->num_sms);
+  const bool splitk = plan.splitk;
   const int kv_rows = f32 ? kBNf : kBN;
   if ((rc = encode_map(&p.tm_q, q, dtype, static_cast<int>(BH), N, D, kBM)) != FA_OK) return rc;
   if ((rc = encode_map(&p.tm_k, k, dtype, static_cast<int>(BH), N, D, kv_rows)) != FA_OK) return rc;
@@ -379,14 +479,6 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   p.lse = lse;
   p.status = info->status_word;
   p.timeout_ns = timeout;
-  p.BH = static_cast<int>(BH);
-  p.N = N;
-  p.num_mb = static_cast<int>((static_cast<long long>(N) + item_rows(splitk) - 1) / item_rows(splitk));
-  p.num_splits = splits;
-  p.num_items = static_cast<int>(BH * p.num_mb * splits);
-  const long long kv_head_bytes = 2ll * N * D * (f32 ? 4 : 2);
-  long long section = kL2SectionBytes / (kv_head_bytes > 0 ? kv_head_bytes : 1);
-  p.section = static_cast<int>(section < 1 ? 1 : (section > BH ? BH : section));
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.force_stall = key.stall;
   if (splits > 1) {
@@ -396,11 +488,19 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   }
 
   // Grid. Persistent (one CTA per SM, items strided in snake order) unless the items have
-  // very unequal cost (causal) and there are several waves of them: then one CTA per item,
-  // dispatched by the hardware in longest-first order, balances better. Split-KV items are
-  // short and even: persistent, so the per-CTA setup is paid once per SM.
-  const bool per_item = causal != 0 && p.num_items > 2 * info->num_sms && splits == 1;
-  const int grid = (per_item || p.num_items < info->num_sms) ? p.num_items : info->num_sms;
+  // very unequal cost (causal) and there are several waves of them: then the static snake
+  // balances badly (the L2 sections interleave long and short items), and each CTA takes the
+  // item list that one-CTA-per-item dispatch would give it (get_schedule), or, without a
+  // schedule, one CTA per item. Split-KV items are short and even: persistent.
+  int grid = (plan.by_dispatch || p.num_items < info->num_sms) ? p.num_items : info->num_sms;
+  p.schedule = nullptr;
+  if (plan.by_dispatch) {
+    const int* sched = get_schedule(dev, p, causal != 0, splitk, f32, info->num_sms, s);
+    if (sched != nullptr) {
+      p.schedule = sched;
+      grid = info->num_sms;
+    }
+  }
 
   LaunchEntry& slot = t_cache[t_cache_next];
   t_cache_next = (t_cache_next + 1) % kCacheSize;
@@ -467,6 +567,23 @@ int fa_set_decomposition(int mode) {
 int fa_debug_force_stall(int on) {
   fa::g_force_stall.store(on != 0 ? 1 : 0);
   return FA_OK;
+}
+
+int fa_debug_work_schedule(int B, int H, int N, int D, int causal, int dtype, int num_sms, int* out, int capacity) {
+  if (B <= 0 || H <= 0 || N <= 0 || num_sms <= 0 || capacity < 0) return FA_ERR_INVALID_ARG;
+  if ((D != 64 && D != 128) || dtype < FA_DTYPE_FP16 || dtype > FA_DTYPE_FP32) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H * ((N + fa::kBM - 1) / fa::kBM) > (1ll << 30)) return FA_ERR_TOO_LARGE;
+  fa::Params p{};
+  const bool f32 = dtype == FA_DTYPE_FP32;
+  const fa::WorkPlan plan = fa::plan_work(p, static_cast<long long>(B) * H, N, D, causal != 0, f32, 1,
+                                          fa::g_decomposition.load(std::memory_order_relaxed), num_sms);
+  if (!plan.by_dispatch) return 0;
+  const std::vector<int> sched = fa::build_schedule(p, causal != 0, plan.splitk, f32, num_sms);
+  const int len = static_cast<int>(sched.size());
+  if (out == nullptr) return len;
+  if (capacity < len) return FA_ERR_INVALID_ARG;
+  std::memcpy(out, sched.data(), sched.size() * sizeof(int));
+  return len;
 }
 
 int fa_check_device_status(void) {

@@ -109,6 +109,9 @@ struct Params {
   int num_mb;                  // row blocks per head: ceil(N / item_rows)
   int num_items;               // BH * num_mb
   int section;                 // causal ordering: heads per L2 section
+  // Work items per CTA, or nullptr for the persistent snake order: gridDim.x + 1 offsets, then
+  // the item indices of CTA c at [offsets[c], offsets[c + 1]) (device memory, read only).
+  const int* schedule;
   float scale_log2;            // scale * log2(e)
   int force_stall;             // test hook: the MMA warp first waits on a barrier nothing arrives on
   // Split-KV partial form only: the K/V tiles of every query tile are divided into num_splits
@@ -195,7 +198,7 @@ struct Item {
 // the head's K/V is read from DRAM about once). Causal: heads are grouped into sections that
 // fit in L2; inside a section the most expensive row blocks (largest mb) come first.
 template <bool CAUSAL>
-__device__ __forceinline__ Item decode_item(int t, const Params& p) {
+__host__ __device__ inline Item decode_item(int t, const Params& p) {
   Item it;
   if (!CAUSAL) {
     it.bh = t / p.num_mb;
@@ -213,7 +216,7 @@ __device__ __forceinline__ Item decode_item(int t, const Params& p) {
 
 // Per work item: nk = K/V tiles loaded, n[w] = K/V tiles processed by warpgroup w (0 = idle).
 template <bool CAUSAL, bool SPLITK>
-__device__ __forceinline__ void tile_counts(int mb, int N, int& nk, int& n0, int& n1) {
+__host__ __device__ inline void tile_counts(int mb, int N, int& nk, int& n0, int& n1) {
   const int nkt = (N + kBN - 1) / kBN;
   if (SPLITK) {
     nk = CAUSAL ? min(mb + 1, nkt) : nkt;
@@ -258,9 +261,14 @@ __device__ __forceinline__ Item decode_work(int t, const Params& p, int& jb, int
   return it;
 }
 
-// k-th work item of this CTA in snake order over the sorted item list (-1 when done). With
-// one CTA per item (gridDim.x == num_items) this is just blockIdx.x.
-__device__ __forceinline__ int item_of(int k, int num_items) {
+// k-th work item of this CTA (-1 when done): from the schedule when there is one, else in
+// snake order over the sorted item list (with one CTA per item, just blockIdx.x).
+__device__ __forceinline__ int item_of(int k, const Params& p) {
+  if (p.schedule != nullptr) {
+    const int b = __ldg(p.schedule + blockIdx.x) + k;
+    return b < __ldg(p.schedule + blockIdx.x + 1) ? __ldg(p.schedule + gridDim.x + 1 + b) : -1;
+  }
+  const int num_items = p.num_items;
   const int G = gridDim.x;
   const long long base = static_cast<long long>(k) * G;
   if (base >= num_items) return -1;
@@ -357,7 +365,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           return true;
         };
         for (int k = 0; ok; ++k) {
-          const int t = item_of(k, p.num_items);
+          const int t = item_of(k, p);
           if (t < 0) break;
           int nk, n0, n1;
           const Item it = decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, jb, nk, n0, n1);
@@ -490,7 +498,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
 
         if (p.force_stall) ok = wait(bar(L::kStall), 0, 12);  // runs out: exercises the abort path
         for (int k = 0; ok; ++k) {
-          const int t = item_of(k, p.num_items);
+          const int t = item_of(k, p);
           if (t < 0) break;
           int jb, nk, n0, n1;
           decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, jb, nk, n0, n1);
@@ -648,7 +656,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
 
         if (p.force_stall) ok = wait(bar(L::kStall), 0, 12);  // runs out: exercises the abort path
         for (int k = 0; ok; ++k) {
-          const int t = item_of(k, p.num_items);
+          const int t = item_of(k, p);
           if (t < 0) break;
           int jb, nk, n0, n1;
           decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, jb, nk, n0, n1);
@@ -797,7 +805,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
-      const int t = item_of(k, p.num_items);
+      const int t = item_of(k, p);
       if (t < 0) break;
       int jb, nk, n0, n1;
       const Item it = decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, jb, nk, n0, n1);

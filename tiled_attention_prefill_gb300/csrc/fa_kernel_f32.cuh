@@ -122,7 +122,7 @@ __device__ __forceinline__ uint32_t to_tf32_for_mma(float x) { return __float_as
 // Key tiles (64 keys) of the item's query tile: all of them, or causally those that hold a
 // key <= the tile's last row; warpgroup w processes tiles j = w, w + 2, ...
 template <bool CAUSAL>
-__device__ __forceinline__ void tile_counts_f32(int qt, int N, int& nk, int& n0, int& n1) {
+__host__ __device__ inline void tile_counts_f32(int qt, int N, int& nk, int& n0, int& n1) {
   const int nkt = (N + kBNf - 1) / kBNf;
   nk = CAUSAL ? min(2 * qt + 2, nkt) : nkt;
   n0 = (nk + 1) >> 1;
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_f32_kernel(const __grid
           return true;
         };
         for (int k = 0; ok; ++k) {
-          const int t = item_of(k, p.num_items);
+          const int t = item_of(k, p);
           if (t < 0) break;
           const Item it = decode_item<CAUSAL>(t, p);
           int nk, n0, n1;
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_f32_kernel(const __grid
       auto release = [&](uint32_t stage) { mma_commit_leader(bar(L::kKEmpty + stage), leader); };
 
       for (int k = 0; ok; ++k) {
-        const int t = item_of(k, p.num_items);
+        const int t = item_of(k, p);
         if (t < 0) break;
         const Item it = decode_item<CAUSAL>(t, p);
         int nk, n0, n1;
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_f32_kernel(const __grid
       uint32_t v_pos = 0, vt_cnt = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int ti = item_of(k, p.num_items);
+        const int ti = item_of(k, p);
         if (ti < 0) break;
         const Item it = decode_item<CAUSAL>(ti, p);
         int nk, n0, n1;
@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_f32_kernel(const __grid
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
-      const int t = item_of(k, p.num_items);
+      const int t = item_of(k, p);
       if (t < 0) break;
       const Item it = decode_item<CAUSAL>(t, p);
       int nk, n0, n1;

@@ -45,6 +45,7 @@ SIGNATURES = {
     "fa_last_cuda_error": (ctypes.c_int, []),
     "fa_set_decomposition": (ctypes.c_int, [ctypes.c_int]),
     "fa_debug_force_stall": (ctypes.c_int, [ctypes.c_int]),
+    "fa_debug_work_schedule": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_int]),
     "fa_forward_splitkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
@@ -126,6 +127,24 @@ def set_decomposition(mode: int) -> None:
 def debug_force_stall(on: bool) -> None:
     """Test hook: following launches stall on purpose so the device-side watchdog fires."""
     _check(load_library().fa_debug_force_stall(1 if on else 0))
+
+
+def debug_work_schedule(B: int, H: int, N: int, D: int, causal: bool, dtype: int, num_sms: int):
+    """The per-CTA work-item lists ``fa_forward`` would use for this shape on ``num_sms`` SMs
+    (host only): a list of ``num_sms`` lists of item indices, or None when the shape's items are
+    strided over the CTAs instead."""
+    lib = load_library()
+    args = (int(B), int(H), int(N), int(D), int(bool(causal)), int(dtype), int(num_sms))
+    n = lib.fa_debug_work_schedule(*args, None, 0)
+    if n < 0:
+        _check(n)
+    if n == 0:
+        return None
+    buf = (ctypes.c_int * n)()
+    _check(min(0, lib.fa_debug_work_schedule(*args, ctypes.addressof(buf), n)))
+    vals = list(buf)
+    off, items = vals[:num_sms + 1], vals[num_sms + 1:]
+    return [items[off[c]:off[c + 1]] for c in range(num_sms)]
 
 
 def forward_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int, N: int, D: int,
