@@ -85,10 +85,6 @@ struct TmemCols {
 };
 static_assert(TmemCols<64>::o(1) + 64 <= kTmemCols && TmemCols<128>::o(1) + 128 <= kTmemCols, "TMEM budget");
 constexpr float kRescaleLog2 = 8.0f;
-#ifndef FA_POLY_PAIRS_PER_8
-#define FA_POLY_PAIRS_PER_8 0
-#endif
-constexpr int kPolyPairsPer8 = FA_POLY_PAIRS_PER_8;  // exp2 column pairs (of 8) computed by polynomial
 constexpr float kLn2 = 0.693147180559945309f;
 
 __host__ __device__ constexpr int item_rows(bool splitk) { return splitk ? kBM : 2 * kBM; }
@@ -863,15 +859,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           for (int i = 0; i < kBN / 4; ++i) {
             const int c = h * (kBN / 4) + i;  // column pair
             const uint64_t x2 = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm2);
-            float p0, p1;
-            if ((c & 7) < kPolyPairsPer8) {
-              f2_unpack(exp2_poly_x2(x2), p0, p1);
-            } else {
-              float x0, x1;
-              f2_unpack(x2, x0, x1);
-              p0 = ex2_approx(x0);
-              p1 = ex2_approx(x1);
-            }
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
             acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
             pk[i] = pack2<BF16>(p0, p1);
           }

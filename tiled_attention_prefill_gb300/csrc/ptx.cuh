@@ -237,33 +237,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
-// 2^x for a packed pair, on the FMA/ALU pipes instead of the MUFU unit.
-// Range reduction: t = x + 1.5*2^23 rounds x to the nearest integer n held in t's low
-// mantissa bits; f = x - n lies in [-1/2, 1/2]. 2^f is a degree-4 polynomial with constant
-// term 1 whose other coefficients come from a Remez exchange fit of the relative error
-// (gen_exp2_poly.py; max relative error 3.6e-6). The result is scaled by 2^n by adding n to
-// the exponent field: bits(t) << 23 equals n << 23 modulo 2^32. x is clamped to -126 so the
-// exponent never underflows (2^-126 is negligible next to the row maximum, which maps to 1).
-__device__ __forceinline__ uint64_t exp2_poly_x2(uint64_t x2) {
-  float a, b;
-  f2_unpack(x2, a, b);
-  const uint64_t x = f2_pack(fmaxf(a, -126.f), fmaxf(b, -126.f));
-  const uint64_t magic = f2_pack(12582912.f, 12582912.f);
-  const uint64_t t = f2_add(x, magic);
-  const uint64_t n = f2_add(t, f2_pack(-12582912.f, -12582912.f));
-  const uint64_t f = f2_fma(n, f2_pack(-1.f, -1.f), x);
-  uint64_t q = f2_fma(f, f2_pack(9.782912210e-03f, 9.782912210e-03f), f2_pack(5.597688258e-02f, 5.597688258e-02f));
-  q = f2_fma(q, f, f2_pack(2.402071059e-01f, 2.402071059e-01f));
-  q = f2_fma(q, f, f2_pack(6.931136250e-01f, 6.931136250e-01f));
-  q = f2_fma(q, f, f2_pack(1.f, 1.f));
-  float q0, q1, t0, t1;
-  f2_unpack(q, q0, q1);
-  f2_unpack(t, t0, t1);
-  uint32_t r0, r1;
-  asm("mad.lo.u32 %0, %1, 8388608, %2;" : "=r"(r0) : "r"(__float_as_uint(t0)), "r"(__float_as_uint(q0)));
-  asm("mad.lo.u32 %0, %1, 8388608, %2;" : "=r"(r1) : "r"(__float_as_uint(t1)), "r"(__float_as_uint(q1)));
-  return f2_pack(__uint_as_float(r0), __uint_as_float(r1));
-}
 // Packs two fp32 values into one 32-bit word of two 16-bit floats (lo in bits 0-15), round to nearest even.
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
