@@ -77,7 +77,11 @@ enum fa_status {
  * enqueues one kernel on `stream`, then returns. O and LSE are valid once the stream has
  * reached that point. Errors are returned before anything is enqueued, except FA_ERR_CUDA
  * for a failed launch and device-side timeouts, which fa_check_device_status() reports.
- * Thread-safe; one-time per-device setup runs on first use.
+ * Thread-safe; one-time per-device setup runs on first use. Causal problems with more than
+ * two waves of work items run on a persistent grid from a per-shape work table. The first
+ * call of such a shape builds the table on the host and copies it synchronously into the
+ * library's module memory (a few KB, no allocation), so it belongs outside stream capture.
+ * A call captured first runs correctly without the table, with one CTA per work item.
  */
 FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
                float scale, int causal, int dtype, void* stream);

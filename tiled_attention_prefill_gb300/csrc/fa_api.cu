@@ -45,6 +45,11 @@ __device__ unsigned int g_device_status = 0;
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// Work schedules of causal multi-wave launches (get_schedule): module memory, filled by a copy
+// on the first call of each shape, so fa_forward allocates nothing.
+constexpr size_t kSchedulePoolInts = size_t(1) << 20;
+static __device__ int g_schedule_pool[kSchedulePoolInts];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -299,7 +304,9 @@ WorkPlan plan_work(Params& p, long long BH, int N, int D, bool causal, bool f32,
 // (decode_item), each item goes to the CTA that frees up first under an estimated cost, the
 // key tiles of its longer warpgroup chain plus a fixed per-item overhead (in tile units). The
 // persistent CTA then prefetches the next item's Q and K/V during the current one, which the
-// per-item launch cannot. Device copies live per device and shape for the process lifetime.
+// per-item launch cannot. The device copies live in a fixed pool of module memory (4 MB per
+// device, a few KB per shape) for the process lifetime; shapes past its end launch one CTA per
+// item.
 struct ScheduleKey {
   int dev, BH, N, causal, splitk, f32, section, num_mb, num_items, grid;
   bool operator<(const ScheduleKey& o) const { return std::memcmp(this, &o, sizeof(ScheduleKey)) < 0; }
@@ -307,6 +314,11 @@ struct ScheduleKey {
 std::mutex g_schedule_mutex;
 std::map<ScheduleKey, int*> g_schedules;
 constexpr double kScheduleItemOverhead = 1.0;
+struct SchedulePool {
+  int* base = nullptr;  // g_schedule_pool on this device
+  size_t used = 0;      // ints handed out
+};
+SchedulePool g_schedule_pools[kMaxDevices];
 
 std::vector<int> build_schedule(const Params& p, bool causal, bool splitk, bool f32, int grid) {
   const int n = p.num_items;
@@ -342,8 +354,9 @@ std::vector<int> build_schedule(const Params& p, bool causal, bool splitk, bool 
   return out;
 }
 
-// The device copy of the schedule for this shape, made on first use (nullptr while the stream is
-// being captured into a graph or when the copy fails: the caller then launches one CTA per item).
+// The device copy of the schedule for this shape, made on first use by a synchronous copy into
+// the pool (nullptr while the stream is being captured into a graph, when the pool is full or
+// when the copy fails: the caller then launches one CTA per item).
 const int* get_schedule(int dev, const Params& p, bool causal, bool splitk, bool f32, int grid, cudaStream_t s) {
   ScheduleKey key{};
   key.dev = dev;
@@ -359,19 +372,23 @@ const int* get_schedule(int dev, const Params& p, bool causal, bool splitk, bool
   std::lock_guard<std::mutex> lock(g_schedule_mutex);
   auto found = g_schedules.find(key);
   if (found != g_schedules.end()) return found->second;
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
-  const std::vector<int> host = build_schedule(p, causal, splitk, f32, grid);
-  int* d = nullptr;
-  if (cudaMalloc(&d, host.size() * sizeof(int)) != cudaSuccess) {
+  SchedulePool& pool = g_schedule_pools[dev];
+  if (pool.base == nullptr && cudaGetSymbolAddress(reinterpret_cast<void**>(&pool.base), g_schedule_pool) != cudaSuccess) {
     cudaGetLastError();
+    pool.base = nullptr;
     return nullptr;
   }
+  const std::vector<int> host = build_schedule(p, causal, splitk, f32, grid);
+  if (pool.used + host.size() > kSchedulePoolInts) return nullptr;
+  int* d = pool.base + pool.used;
   if (cudaMemcpy(d, host.data(), host.size() * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
     cudaGetLastError();
-    cudaFree(d);
     return nullptr;
   }
+  pool.used += host.size();
   g_schedules[key] = d;
   return d;
 }
