@@ -23,7 +23,8 @@
 //     warpgroups (208 each); 88 + 2 * 208 = 3 * 168, the launch allocation. At D = 64 every
 //     role fits in the launch allocation and no split is made.
 //   * K and V tiles (128 keys x D) stream through a shared-memory ring filled by TMA
-//     (128-byte swizzle) in exactly the order the MMA warp consumes them.
+//     (128-byte swizzle) in exactly the order the MMA warp consumes them. Single-query-tile
+//     items leave the second Q tile free, and the ring starts there, one stage deeper.
 //   * S = Q K^T for a warpgroup goes to its own 128 TMEM columns (fp32). The warpgroup reads
 //     its row of S (tcgen05.ld), writes P as fp16/bf16 back into the same columns, and the MMA
 //     warp computes O += P V with P read from TMEM. O (fp32, D columns per warpgroup) stays in
@@ -119,14 +120,16 @@ struct Params {
   CUtensorMap tm_op;  // o_part as 3-D fp32 (D, N, num_splits * BH), box (32, 32, 1), 128B swizzle
 };
 
-template <int D>
+// kRingInQ1: single-query-tile items that stage nothing in the second Q tile (not the split-KV
+// partial form) start the K/V ring there, one stage deeper.
+template <int D, bool kRingInQ1 = false>
 struct SmemLayout {
   static constexpr int kChunks = D / 64;           // 64-column (128-byte) swizzle chunks per row
   static constexpr int kChunkBytes = kBM * 128;    // one chunk of a 128-row tile
   static constexpr int kTileBytes = kBM * D * 2;   // a 128 x D fp16/bf16 tile
-  static constexpr int kStages = (D == 64) ? 6 : 3;
+  static constexpr int kStages = ((D == 64) ? 6 : 3) + (kRingInQ1 ? 1 : 0);
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQOff + 2 * kTileBytes;
+  static constexpr int kKVOff = kQOff + (kRingInQ1 ? 1 : 2) * kTileBytes;
   static constexpr int kOOff = kKVOff + kStages * kTileBytes;  // two staging tiles for O
   static constexpr int kBarOff = kOOff + 2 * kTileBytes;
   // barrier indices
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
   // issuer is faster (two made c4 8%, c5 10% and the short causal c2 7% slower).
   constexpr bool kDualMma = (D == 64) && !SPLITK;
   constexpr uint32_t kMmaIssuers = kDualMma ? 2 : 1;
-  using L = SmemLayout<D>;
+  using L = SmemLayout<D, SPLITK && !PARTIAL>;
   using TC = TmemCols<D>;
   constexpr bool kSepP = TC::kSepP;
   constexpr int kItemRows = item_rows(SPLITK);
