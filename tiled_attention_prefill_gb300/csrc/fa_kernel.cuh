@@ -24,7 +24,8 @@
 //     role fits in the launch allocation and no split is made.
 //   * K and V tiles (128 keys x D) stream through a shared-memory ring filled by TMA
 //     (128-byte swizzle) in exactly the order the MMA warp consumes them. Single-query-tile
-//     items leave the second Q tile free, and the ring starts there, one stage deeper.
+//     items leave the second Q tile free, and the ring starts there, one stage deeper; at
+//     D = 128 two-query-tile items stage O one 64-column chunk at a time for a fourth stage.
 //   * S = Q K^T for a warpgroup goes to its own 128 TMEM columns (fp32). The warpgroup reads
 //     its row of S (tcgen05.ld), writes P as fp16/bf16 back into the same columns, and the MMA
 //     warp computes O += P V with P read from TMEM. O (fp32, D columns per warpgroup) stays in
@@ -121,17 +122,21 @@ struct Params {
 };
 
 // kRingInQ1: single-query-tile items that stage nothing in the second Q tile (not the split-KV
-// partial form) start the K/V ring there, one stage deeper.
-template <int D, bool kRingInQ1 = false>
+// partial form) start the K/V ring there, one stage deeper. kHalfStaging (two-query-tile
+// items): at D = 128 each warpgroup stages one 64-column chunk of O at a time, and the space
+// saved is a fourth K/V stage.
+template <int D, bool kRingInQ1 = false, bool kHalfStaging = false>
 struct SmemLayout {
   static constexpr int kChunks = D / 64;           // 64-column (128-byte) swizzle chunks per row
   static constexpr int kChunkBytes = kBM * 128;    // one chunk of a 128-row tile
   static constexpr int kTileBytes = kBM * D * 2;   // a 128 x D fp16/bf16 tile
-  static constexpr int kStages = ((D == 64) ? 6 : 3) + (kRingInQ1 ? 1 : 0);
+  static constexpr bool kOneChunkStaging = kHalfStaging && kChunks > 1;
+  static constexpr int kStages = ((D == 64) ? 6 : 3) + (kRingInQ1 ? 1 : 0) + (kOneChunkStaging ? 1 : 0);
+  static constexpr int kOStageBytes = kOneChunkStaging ? kChunkBytes : kTileBytes;  // per warpgroup
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + (kRingInQ1 ? 1 : 2) * kTileBytes;
-  static constexpr int kOOff = kKVOff + kStages * kTileBytes;  // two staging tiles for O
-  static constexpr int kBarOff = kOOff + 2 * kTileBytes;
+  static constexpr int kOOff = kKVOff + kStages * kTileBytes;  // two staging areas for O
+  static constexpr int kBarOff = kOOff + 2 * kOStageBytes;
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kQEmpty = 1;
@@ -148,7 +153,8 @@ struct SmemLayout {
   static constexpr int kDrain = kStall + 1;          // [2] per MMA warp
   static constexpr int kNumBars = kDrain + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kStatsOff = kMiscOff + 16;  // split-K (m, l) hand-off, 2 x 128 fp32
+  static constexpr int kBytes = kStatsOff + 2 * kBM * 4;
   static constexpr int kDynamicBytes = kBytes + 1024;  // slack to align the base to 1024 bytes
   static_assert(kDynamicBytes <= 232448, "shared memory budget");
 };
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
   // issuer is faster (two made c4 8%, c5 10% and the short causal c2 7% slower).
   constexpr bool kDualMma = (D == 64) && !SPLITK;
   constexpr uint32_t kMmaIssuers = kDualMma ? 2 : 1;
-  using L = SmemLayout<D, SPLITK && !PARTIAL>;
+  using L = SmemLayout<D, SPLITK && !PARTIAL, !SPLITK>;
   using TC = TmemCols<D>;
   constexpr bool kSepP = TC::kSepP;
   constexpr int kItemRows = item_rows(SPLITK);
@@ -298,9 +304,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
   auto bar = [&](int idx) -> uint32_t { return sbase + L::kBarOff + 8u * idx; };
   auto q_addr = [&](int i) -> uint32_t { return sbase + L::kQOff + i * L::kTileBytes; };
   auto kv_addr = [&](int s) -> uint32_t { return sbase + L::kKVOff + s * L::kTileBytes; };
-  auto o_addr = [&](int i) -> uint32_t { return sbase + L::kOOff + i * L::kTileBytes; };
-  // split-K: warpgroup 1 never stages O, so its staging tile carries the (m, l) hand-off
-  float* stats_m = reinterpret_cast<float*>(smem + L::kOOff + L::kTileBytes);
+  auto o_addr = [&](int i) -> uint32_t { return sbase + L::kOOff + i * L::kOStageBytes; };
+  float* stats_m = reinterpret_cast<float*>(smem + L::kStatsOff);
   float* stats_l = stats_m + kBM;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
@@ -1023,8 +1028,23 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           }
           continue;
         }
+        if constexpr (L::kOneChunkStaging) {
+          if (c > 0 && (c & 63) == 0) {
+            // Store the previous 64-column chunk; its reads must finish before the staging
+            // area is written again.
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int row0 = qt * kBM + wq * 32;
+            if (lane == 0 && row0 < p.N) {
+              tma_store_3d(&p.tm_o, ob + wq * 32 * 128, c - 64, row0, it.bh);
+              bulk_commit_group();
+              bulk_wait_group_read0();
+            }
+            __syncwarp();
+          }
+        }
         // 16-byte units (8 columns) of the 128-byte swizzled row of the 64-column chunk.
-        const uint32_t row_base = ob + (c >> 6) * L::kChunkBytes + r * 128;
+        const uint32_t row_base = ob + (L::kOneChunkStaging ? 0 : (c >> 6) * L::kChunkBytes) + r * 128;
 #pragma unroll
         for (int u = 0; u < kEpi / 8; ++u) {
           const int unit = ((c & 63) >> 3) + u;
@@ -1058,8 +1078,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
       __syncwarp();
       const int row0_warp = qt * kBM + wq * 32;
       if (lane == 0 && row0_warp < p.N) {  // rows past N are clipped by the store; skip empty boxes
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_store_3d(&p.tm_o, ob + c * L::kChunkBytes + wq * 32 * 128, c * 64, row0_warp, it.bh);
+        if constexpr (L::kOneChunkStaging) {
+          tma_store_3d(&p.tm_o, ob + wq * 32 * 128, D - 64, row0_warp, it.bh);
+        } else {
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_store_3d(&p.tm_o, ob + c * L::kChunkBytes + wq * 32 * 128, c * 64, row0_warp, it.bh);
+        }
         bulk_commit_group();
       }
     }
