@@ -131,7 +131,7 @@ struct SmemLayout {
   static constexpr int kChunkBytes = kBM * 128;    // one chunk of a 128-row tile
   static constexpr int kTileBytes = kBM * D * 2;   // a 128 x D fp16/bf16 tile
   static constexpr bool kOneChunkStaging = kHalfStaging && kChunks > 1;
-  static constexpr int kStages = ((D == 64) ? 6 : 3) + (kRingInQ1 ? 1 : 0) + (kOneChunkStaging ? 1 : 0);
+  static constexpr int kStages = ((D == 64) ? 8 : 3) + (kRingInQ1 ? 1 : 0) + (kOneChunkStaging ? 1 : 0);
   static constexpr int kOStageBytes = kOneChunkStaging ? kChunkBytes : kTileBytes;  // per warpgroup
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + (kRingInQ1 ? 1 : 2) * kTileBytes;
