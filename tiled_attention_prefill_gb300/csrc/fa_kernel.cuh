@@ -121,8 +121,8 @@ struct Params {
   CUtensorMap tm_op;  // o_part as 3-D fp32 (D, N, num_splits * BH), box (32, 32, 1), 128B swizzle
 };
 
-// kRingInQ1: single-query-tile items that stage nothing in the second Q tile (not the split-KV
-// partial form) start the K/V ring there, one stage deeper. kHalfStaging (two-query-tile
+// kRingInQ1: single-query-tile items leave the second Q tile unused, and the K/V ring starts
+// there, one stage deeper. kHalfStaging (two-query-tile
 // items): at D = 128 each warpgroup stages one 64-column chunk of O at a time, and the space
 // saved is a fourth K/V stage.
 template <int D, bool kRingInQ1 = false, bool kHalfStaging = false>
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
   // issuer is faster (two made c4 8%, c5 10% and the short causal c2 7% slower).
   constexpr bool kDualMma = (D == 64) && !SPLITK;
   constexpr uint32_t kMmaIssuers = kDualMma ? 2 : 1;
-  using L = SmemLayout<D, SPLITK && !PARTIAL, !SPLITK>;
+  using L = SmemLayout<D, SPLITK, !SPLITK>;
   using TC = TmemCols<D>;
   constexpr bool kSepP = TC::kSepP;
   constexpr int kItemRows = item_rows(SPLITK);
@@ -990,10 +990,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
       const float c_self = a_self * inv_l, c_other = a_other * inv_l;
       const uint32_t ob = o_addr(wg);
       // Split-KV partial form: warp wq's fp32 boxes go to its quarter of the O staging tile of
-      // warpgroup 0, then to its quarter of the second Q tile (single query tiles leave it unused).
+      // warpgroup 0, then to its quarter of warpgroup 1's (which stages nothing in this form).
       auto part_box = [&](int b) -> uint32_t {
         constexpr int kPerRegion = D / 64;  // 4 KB boxes per quarter tile
-        const uint32_t region = b < kPerRegion ? o_addr(0) : q_addr(1);
+        const uint32_t region = b < kPerRegion ? o_addr(0) : o_addr(1);
         return region + wq * (L::kTileBytes / 4) + (b % kPerRegion) * 4096;
       };
       // Columns per step: 64 (one 128-byte swizzle chunk) at D = 64; 32 at D = 128, where the

@@ -12,7 +12,7 @@ namespace fa {
 
 template <int D, bool BF16, bool CAUSAL, bool SPLITK, bool PARTIAL = false>
 cudaError_t launch_forward(const Params& p, int grid, cudaStream_t stream) {
-  using L = SmemLayout<D, SPLITK && !PARTIAL, !SPLITK>;
+  using L = SmemLayout<D, SPLITK, !SPLITK>;
   auto kernel = fa_fwd_kernel<D, BF16, CAUSAL, SPLITK, PARTIAL>;
   // Opt in to the large dynamic shared-memory carve-out once per device.
   static std::atomic<unsigned long long> configured{0};
