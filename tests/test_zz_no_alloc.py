@@ -40,3 +40,16 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(name, splits):
     assert torch.equal(a1, r1) and torch.equal(la1, lr1)
     assert torch.equal(a2, r2) and torch.equal(la2, lr2)
     assert not torch.equal(a1, a2)
+
+
+@pytest.mark.gpu
+def test_one_split_causal_multiwave_matches_fa_forward():
+    # One split runs the fused forward; this causal shape has more than two waves of work
+    # items, so it also exercises the per-shape work table that lives in module memory.
+    w = workloads.WORKLOADS["c4"]
+    q, k, v = (x.cuda() for x in workloads.make_qkv(w))
+    a, la = fa.forward_splitkv_noalloc(q, k, v, causal=True, scale=w.scale, num_splits=1)
+    r, lr = fa.forward(q, k, v, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    assert torch.equal(a, r) and torch.equal(la, lr)
