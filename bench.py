@@ -207,7 +207,8 @@ def run_reference(args, w):
         times.append(el)
     value = statistics.mean(rates)
     flops_step = heads_per_step * (4.0 * w.N * w.N * w.D / (2 if w.causal else 1))
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+    # n_gpus is the launch's N (the same as the GPU arm's line); the work runs on rank 0's host cores
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_desc(w),
