@@ -238,10 +238,20 @@ FA_API int fa_set_watchdog_ns(unsigned long long ns);
  *   FA_DECOMP_SPLIT_KV (2)  each work item is one 128-row query tile whose K/V tiles are split
  *                           between the two softmax warpgroups and merged at the end (twice
  *                           the items, half the serial chain: for short or few sequences).
- * All three compute the same result (up to floating-point rounding order). Returns FA_OK or
+ *                           A causal launch at D = 64 with between one and two such items
+ *                           per SM runs them in pairs: each CTA takes a long and a short query
+ *                           tile at once and divides their K/V tiles evenly between the
+ *                           warpgroups;
+ *   FA_DECOMP_SPLIT_KV_SERIAL (3)  the same items, never paired (one after another).
+ * All four compute the same result (up to floating-point rounding order). Returns FA_OK or
  * FA_ERR_INVALID_ARG for an unknown value.
  */
-enum fa_decomposition { FA_DECOMP_AUTO = 0, FA_DECOMP_TWO_TILES = 1, FA_DECOMP_SPLIT_KV = 2 };
+enum fa_decomposition {
+  FA_DECOMP_AUTO = 0,
+  FA_DECOMP_TWO_TILES = 1,
+  FA_DECOMP_SPLIT_KV = 2,
+  FA_DECOMP_SPLIT_KV_SERIAL = 3
+};
 FA_API int fa_set_decomposition(int mode);
 
 /*
@@ -268,6 +278,26 @@ FA_API int fa_debug_force_stall(int on);
  */
 FA_API int fa_debug_work_schedule(int B, int H, int N, int D, int causal, int dtype, int num_sms, int* out,
                                   int capacity);
+
+/*
+ * Inspection hook for the work decomposition (host only, no CUDA call) of a fa_forward of
+ * this shape on a GPU with num_sms SMs, with the current fa_set_decomposition mode.
+ * plan[0..4] (required) receive: the number of work items; 1 if an item is one 128-row
+ * query tile (else two); 1 if the launch is paired; 1 if it follows a dispatch-order
+ * schedule (fa_debug_work_schedule); the grid size (with a schedule: num_sms). A paired
+ * launch is causal, fp16 or bf16 at D = 64, with single-query-tile items, more than num_sms
+ * and at most 2 num_sms of them: CTA c of a grid of G runs items c and 2 G - 1 - c at once.
+ * For a paired launch,
+ * units (when not NULL) receives 6 ints per CTA: item a (the one with more K/V tiles), item
+ * b (-1 when the CTA has one item), the K/V tiles of a and of b, and the tiles warpgroup 0
+ * and warpgroup 1 process (warpgroup 0 takes a's first ones; warpgroup 1 all of b, then the
+ * rest of a). Returns the number of unit ints (6 G; 0 when not paired), the same count
+ * without writing when units is NULL, FA_ERR_INVALID_ARG for bad sizes, a NULL plan or a
+ * too small capacity, FA_ERR_UNSUPPORTED for D or dtype, FA_ERR_TOO_LARGE past the item
+ * limit.
+ */
+FA_API int fa_debug_work_plan(int B, int H, int N, int D, int causal, int dtype, int num_sms, int* plan, int* units,
+                              int capacity);
 
 /* The cudaError_t value behind the most recent FA_ERR_CUDA returned on this host thread. */
 FA_API int fa_last_cuda_error(void);

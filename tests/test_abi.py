@@ -121,7 +121,8 @@ def test_missing_library_fails_loudly(tmp_path):
 def test_decomposition_setter(lib):
     assert lib.fa_set_decomposition(1) == fa.FA_OK
     assert lib.fa_set_decomposition(2) == fa.FA_OK
-    assert lib.fa_set_decomposition(3) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_set_decomposition(3) == fa.FA_OK
+    assert lib.fa_set_decomposition(4) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_set_decomposition(-1) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_set_decomposition(0) == fa.FA_OK
 

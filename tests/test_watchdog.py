@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("name,decomp", [("c3", fa.FA_DECOMP_TWO_TILES), ("c2", fa.FA_DECOMP_SPLIT_KV),
-                                         ("c4", fa.FA_DECOMP_AUTO)])
+                                         ("c2", fa.FA_DECOMP_SPLIT_KV_SERIAL), ("c4", fa.FA_DECOMP_AUTO)])
 def test_watchdog_timeout_reported_and_context_survives(name, decomp):
     w = workloads.WORKLOADS[name]
     q, k, v = (x.cuda() for x in workloads.make_qkv(w))

@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["fa_api.cu", "fa_inst_d64.cu", "fa_inst_d128.cu", "fa_inst_partial.cu", "fa_merge.cu", "fa_naive.cu", "fa_inst_f32.cu"]
+SOURCES = ["fa_api.cu", "fa_inst_d64.cu", "fa_inst_d128.cu", "fa_inst_partial.cu", "fa_inst_pair.cu", "fa_merge.cu", "fa_naive.cu", "fa_inst_f32.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Only the fa_* C entry points are exported (FA_API); everything else stays hidden so that two
 # copies of the library, or another library with the same C++ names, cannot interpose.

@@ -36,6 +36,8 @@ FA_DECLARE_LAUNCH_PARTIAL(extern, 128, false, false)
 FA_DECLARE_LAUNCH_PARTIAL(extern, 128, false, true)
 FA_DECLARE_LAUNCH_PARTIAL(extern, 128, true, false)
 FA_DECLARE_LAUNCH_PARTIAL(extern, 128, true, true)
+FA_DECLARE_LAUNCH_PAIR(extern, 64, false, true)
+FA_DECLARE_LAUNCH_PAIR(extern, 64, true, true)
 
 // Error bits OR-ed in by kernels of this library on the device they ran on.
 __device__ unsigned int g_device_status = 0;
@@ -166,6 +168,7 @@ struct LaunchEntry {
   Params params;
   int grid;
   bool splitk;
+  bool pair;       // paired split-K form
   bool f32;        // fp32-I/O (tf32) kernel
   int splits;      // > 1: split-KV partial kernel, then the merge
   void* o;         // merge output
@@ -192,7 +195,10 @@ cudaError_t launch_partial(const Params& p, int grid, int D, bool bf16, bool c, 
   return c ? launch_forward<128, true, true, true, true>(p, grid, s) : launch_forward<128, true, false, true, true>(p, grid, s);
 }
 
-cudaError_t launch(const Params& p, int grid, bool splitk, int D, bool bf16, bool c, cudaStream_t s) {
+cudaError_t launch(const Params& p, int grid, bool splitk, bool pair, int D, bool bf16, bool c, cudaStream_t s) {
+  if (pair && c && D == 64)
+    return bf16 ? launch_forward<64, true, true, true, false, true>(p, grid, s)
+                : launch_forward<64, false, true, true, false, true>(p, grid, s);
 #define FA_LAUNCH(DD, BB, CC) \
   (splitk ? launch_forward<DD, BB, CC, true>(p, grid, s) : launch_forward<DD, BB, CC, false>(p, grid, s))
   if (D == 64) {
@@ -271,10 +277,11 @@ int choose_splits(long long BH, int N, int D, bool causal, int num_sms) {
 struct WorkPlan {
   bool splitk;       // single-query-tile items
   bool by_dispatch;  // causal with more than two waves of items: items follow dispatch order
+  bool pair;         // causal single-query-tile items, one to two per SM: each CTA runs two at once
 };
 WorkPlan plan_work(Params& p, long long BH, int N, int D, bool causal, bool f32, int splits, int decomp, int num_sms) {
   const long long items_two = BH * ((static_cast<long long>(N) + item_rows(false) - 1) / item_rows(false));
-  bool splitk = decomp == FA_DECOMP_SPLIT_KV || splits > 1 || f32;
+  bool splitk = decomp == FA_DECOMP_SPLIT_KV || decomp == FA_DECOMP_SPLIT_KV_SERIAL || splits > 1 || f32;
   if (decomp == FA_DECOMP_AUTO && splits == 1 && !f32) {
     if (causal) {
       // Unequal item costs are balanced by dispatch order; split only when the GPU is not full.
@@ -297,7 +304,11 @@ WorkPlan plan_work(Params& p, long long BH, int N, int D, bool causal, bool f32,
   const long long kv_head_bytes = 2ll * N * D * (f32 ? 4 : 2);
   const long long section = kL2SectionBytes / (kv_head_bytes > 0 ? kv_head_bytes : 1);
   p.section = static_cast<int>(section < 1 ? 1 : (section > BH ? BH : section));
-  return WorkPlan{splitk, causal && p.num_items > 2 * num_sms && splits == 1};
+  // Pairs at D = 64 only: c2 13.25 -> 12.55 us. At D = 128 the paired form measured 2-3% slower
+  // (warpgroup 1's store of b, in the middle of its chain, stalls the single MMA issuer).
+  const bool pair = splitk && causal && D == 64 && splits == 1 && !f32 && decomp != FA_DECOMP_SPLIT_KV_SERIAL &&
+                    p.num_items > num_sms && p.num_items <= 2 * num_sms;
+  return WorkPlan{splitk, causal && p.num_items > 2 * num_sms && splits == 1, pair};
 }
 
 // Item lists for a persistent grid that follow the one-CTA-per-item dispatch: in item order
@@ -471,7 +482,7 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
           e = launch_merge(c.params.o_part, kPartsF32, c.params.lse_part, c.splits, c.rows, D, c.o, bf16, c.lse,
                            c.num_sms, s);
       } else {
-        e = launch(c.params, c.grid, c.splitk, D, bf16, key.causal != 0, s);
+        e = launch(c.params, c.grid, c.splitk, c.pair, D, bf16, key.causal != 0, s);
       }
       return e == cudaSuccess ? FA_OK : cuda_fail(e);
     }
@@ -508,7 +519,8 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   // very unequal cost (causal) and there are several waves of them: then the static snake
   // balances badly (the L2 sections interleave long and short items), and each CTA takes the
   // item list that one-CTA-per-item dispatch would give it (get_schedule), or, without a
-  // schedule, one CTA per item. Split-KV items are short and even: persistent.
+  // schedule, one CTA per item. Split-KV items are short and even: persistent. Paired
+  // split-K launches also take one CTA per SM: CTA c runs items c and 2 grid - 1 - c.
   int grid = (plan.by_dispatch || p.num_items < info->num_sms) ? p.num_items : info->num_sms;
   p.schedule = nullptr;
   if (plan.by_dispatch) {
@@ -525,6 +537,7 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   slot.params = p;
   slot.grid = grid;
   slot.splitk = splitk;
+  slot.pair = plan.pair;
   slot.f32 = f32;
   slot.splits = splits;
   slot.o = o;
@@ -539,7 +552,7 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
     if (e == cudaSuccess)
       e = launch_merge(p.o_part, kPartsF32, p.lse_part, splits, BH * N, D, o, bf16, lse, info->num_sms, s);
   } else {
-    e = launch(p, grid, splitk, D, bf16, causal != 0, s);
+    e = launch(p, grid, splitk, plan.pair, D, bf16, causal != 0, s);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
@@ -576,7 +589,9 @@ int fa_set_watchdog_ns(unsigned long long ns) {
 }
 
 int fa_set_decomposition(int mode) {
-  if (mode != FA_DECOMP_AUTO && mode != FA_DECOMP_TWO_TILES && mode != FA_DECOMP_SPLIT_KV) return FA_ERR_INVALID_ARG;
+  if (mode != FA_DECOMP_AUTO && mode != FA_DECOMP_TWO_TILES && mode != FA_DECOMP_SPLIT_KV &&
+      mode != FA_DECOMP_SPLIT_KV_SERIAL)
+    return FA_ERR_INVALID_ARG;
   fa::g_decomposition.store(mode);
   return FA_OK;
 }
@@ -600,6 +615,44 @@ int fa_debug_work_schedule(int B, int H, int N, int D, int causal, int dtype, in
   if (out == nullptr) return len;
   if (capacity < len) return FA_ERR_INVALID_ARG;
   std::memcpy(out, sched.data(), sched.size() * sizeof(int));
+  return len;
+}
+
+int fa_debug_work_plan(int B, int H, int N, int D, int causal, int dtype, int num_sms, int* plan, int* units,
+                       int capacity) {
+  if (B <= 0 || H <= 0 || N <= 0 || num_sms <= 0 || capacity < 0 || plan == nullptr) return FA_ERR_INVALID_ARG;
+  if ((D != 64 && D != 128) || dtype < FA_DTYPE_FP16 || dtype > FA_DTYPE_FP32) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H * ((N + fa::kBM - 1) / fa::kBM) > (1ll << 30)) return FA_ERR_TOO_LARGE;
+  fa::Params p{};
+  const bool f32 = dtype == FA_DTYPE_FP32;
+  const fa::WorkPlan wp = fa::plan_work(p, static_cast<long long>(B) * H, N, D, causal != 0, f32, 1,
+                                        fa::g_decomposition.load(std::memory_order_relaxed), num_sms);
+  const int grid = (wp.by_dispatch || p.num_items > num_sms) ? num_sms : p.num_items;
+  plan[0] = p.num_items;
+  plan[1] = wp.splitk ? 1 : 0;
+  plan[2] = wp.pair ? 1 : 0;
+  plan[3] = wp.by_dispatch ? 1 : 0;
+  plan[4] = grid;
+  if (!wp.pair) return 0;
+  const int len = 6 * grid;
+  if (units == nullptr) return len;
+  if (capacity < len) return FA_ERR_INVALID_ARG;
+  for (int c = 0; c < grid; ++c) {
+    fa::Unit U{};
+    int ta = -1, tb = -1;
+    int* u = units + 6 * c;
+    if (!fa::pair_unit<true>(c, grid, p, U, &ta, &tb)) {
+      u[0] = u[1] = -1;
+      u[2] = u[3] = u[4] = u[5] = 0;
+      continue;
+    }
+    u[0] = ta;
+    u[1] = tb;
+    u[2] = U.nk - U.nb;
+    u[3] = U.nb;
+    u[4] = U.n0;
+    u[5] = U.n1;
+  }
   return len;
 }
 

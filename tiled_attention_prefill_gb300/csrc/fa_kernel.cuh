@@ -149,7 +149,9 @@ struct SmemLayout {
   static constexpr int kPVDone = kSFree + 2;         // [2] each PV of warpgroup i completed (separate-P form)
   static constexpr int kStats = kPVDone + 2;         // split-K: warpgroup 1 published (m, l)
   static constexpr int kO1Free = kStats + 1;         // split-K: warpgroup 0 finished reading O1
-  static constexpr int kStall = kO1Free + 1;         // never arrived on (watchdog test hook)
+  static constexpr int kO1Self = kO1Free + 1;        // paired: warpgroup 1 finished reading O1 for its own store
+  static constexpr int kOFullB = kO1Self + 1;        // paired: last PV of warpgroup 1's own query tile completed
+  static constexpr int kStall = kOFullB + 1;         // never arrived on (watchdog test hook)
   static constexpr int kDrain = kStall + 1;          // [2] per MMA warp
   static constexpr int kNumBars = kDrain + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -158,6 +160,12 @@ struct SmemLayout {
   static constexpr int kDynamicBytes = kBytes + 1024;  // slack to align the base to 1024 bytes
   static_assert(kDynamicBytes <= 232448, "shared memory budget");
 };
+
+// Layout of a kernel instance. Single-query-tile items run the ring into the unused second
+// Q tile; two-query-tile items and paired split-K units hold two Q tiles and, at D = 128,
+// stage O one chunk at a time.
+template <int D, bool SPLITK, bool PAIR>
+using KernelLayout = SmemLayout<D, SPLITK && !PAIR, !SPLITK || PAIR>;
 
 struct Watch {
   volatile int* abort_flag;
@@ -282,16 +290,96 @@ __device__ __forceinline__ int item_of(int k, const Params& p) {
   return t < num_items ? static_cast<int>(t) : -1;
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SPLITK, bool PARTIAL>
+// The work of one pass through a CTA's loops. Two-query-tile and unpaired single-query-tile
+// forms: one work item `a` (decode_work), whose K/V positions [0, nk) are its tiles jb + j;
+// in the split-K form position j belongs to warpgroup j & 1 as its tile u = j >> 1.
+// Paired split-K form (a launch with between one and two items per CTA): CTA c runs items c
+// and 2 G - 1 - c of the sorted list together, `a` the one with more key tiles (na >= nb).
+// Warpgroup 0 takes a's first n0 = ceil((na + nb) / 2) tiles; warpgroup 1 takes all nb
+// tiles of b, stores b itself, then takes a's remaining n1 - nb tiles, which warpgroup 0
+// merges as in the split-K form. Each warpgroup then runs n0 or n0 - 1 tiles, where two
+// items one after another would run ceil(na / 2) + ceil(nb / 2) tiles and an item change.
+struct Unit {
+  Item a, b;
+  int jb;          // first K/V tile of a's range (split-KV partial form)
+  int nk;          // K/V positions: na, or na + nb when paired
+  int n0, n1;      // tiles of warpgroup 0 and 1
+  int nb;          // tiles of b (0: not paired)
+};
+
+// The paired unit of CTA c of G (items c and 2 G - 1 - c; false when c has no item).
+template <bool CAUSAL>
+__host__ __device__ inline bool pair_unit(int c, int G, const Params& p, Unit& U, int* ta_out = nullptr,
+                                          int* tb_out = nullptr) {
+  int ta = c, tb = 2 * G - 1 - c;
+  if (ta >= p.num_items) return false;
+  U.a = decode_item<CAUSAL>(ta, p);
+  U.a.split = 0;
+  int na, nb = 0, x0, x1;
+  tile_counts<CAUSAL, true>(U.a.mb, p.N, na, x0, x1);
+  if (tb < p.num_items) {
+    U.b = decode_item<CAUSAL>(tb, p);
+    U.b.split = 0;
+    tile_counts<CAUSAL, true>(U.b.mb, p.N, nb, x0, x1);
+    if (nb > na) {
+      const Item t = U.a;
+      U.a = U.b;
+      U.b = t;
+      const int n = na;
+      na = nb;
+      nb = n;
+      const int tt = ta;
+      ta = tb;
+      tb = tt;
+    }
+  } else {
+    tb = -1;
+  }
+  U.jb = 0;
+  U.nk = na + nb;
+  U.n0 = (U.nk + 1) >> 1;
+  U.n1 = U.nk >> 1;
+  U.nb = nb;
+  if (ta_out != nullptr) *ta_out = ta;
+  if (tb_out != nullptr) *tb_out = tb;
+  return true;
+}
+
+template <bool CAUSAL, bool SPLITK, bool PARTIAL, bool PAIR>
+__device__ __forceinline__ bool decode_unit(int k, const Params& p, Unit& U) {
+  if constexpr (PAIR) {
+    return k == 0 && pair_unit<CAUSAL>(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), p, U);
+  } else {
+    const int t = item_of(k, p);
+    if (t < 0) return false;
+    U.a = decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, U.jb, U.nk, U.n0, U.n1);
+    U.nb = 0;
+    return true;
+  }
+}
+
+// Split-K form: the K/V tile of warpgroup w's u-th position, and whether it is one of b's.
+template <bool PAIR>
+__device__ __forceinline__ int unit_tile(const Unit& U, int w, int u, bool& from_b) {
+  from_b = false;
+  if (!PAIR || U.nb == 0) return U.jb + 2 * u + w;
+  if (w == 0) return u;
+  from_b = u < U.nb;
+  return from_b ? u : U.n0 + (u - U.nb);
+}
+
+template <int D, bool BF16, bool CAUSAL, bool SPLITK, bool PARTIAL, bool PAIR = false>
 __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   static_assert(!PARTIAL || SPLITK, "the split-KV partial form uses one query tile per item");
+  static_assert(!PAIR || (SPLITK && !PARTIAL), "pairs are formed from whole single-query-tile items");
+  static_assert(!PAIR || TmemCols<D>::kSepP, "pairs use the separate-P split-K issue order (D = 64)");
   constexpr bool kRegSplit = reg_split<D>();
   // Two MMA issuers (one per softmax warpgroup) where that measured faster: D = 64 with two
   // query tiles per item (c3 43.2 -> 40.5 us). At D = 128 and with single query tiles one
   // issuer is faster (two made c4 8%, c5 10% and the short causal c2 7% slower).
   constexpr bool kDualMma = (D == 64) && !SPLITK;
   constexpr uint32_t kMmaIssuers = kDualMma ? 2 : 1;
-  using L = SmemLayout<D, SPLITK, !SPLITK>;
+  using L = KernelLayout<D, SPLITK, PAIR>;
   using TC = TmemCols<D>;
   constexpr bool kSepP = TC::kSepP;
   constexpr int kItemRows = item_rows(SPLITK);
@@ -327,6 +415,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
     }
     mbar_init(bar(L::kStats), kBM);
     mbar_init(bar(L::kO1Free), kBM);
+    mbar_init(bar(L::kO1Self), kBM);
+    mbar_init(bar(L::kOFullB), 1);
     mbar_init(bar(L::kStall), 1);
     mbar_init(bar(L::kDrain), 1);
     mbar_init(bar(L::kDrain + 1), 1);
@@ -358,30 +448,38 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
       if (lane == 0) {
         uint32_t kv_pos = 0, q_loads = 0;
         bool ok = true;
-        int jb = 0;  // first K/V tile of the current item
-        auto load_kv = [&](const void* tm, int j, int bh) -> bool {
+        Unit U{};
+        // K/V tile of position j of the current unit into the next ring slot.
+        auto load_kv = [&](const void* tm, int j) -> bool {
+          int jt = U.jb + j, bh = U.a.bh;
+          if (SPLITK) {
+            bool from_b;
+            jt = unit_tile<PAIR>(U, j & 1, j >> 1, from_b);
+            if (from_b) bh = U.b.bh;
+          }
           const uint32_t s = kv_pos % L::kStages;
           if (!wait_phase(bar(L::kKVEmpty + s), ((kv_pos / L::kStages) & 1) ^ 1, watch, 1)) return false;
           mbar_arrive_expect_tx(bar(L::kKVFull + s), L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(kv_addr(s) + c * L::kChunkBytes, tm, bar(L::kKVFull + s), c * 64, (jb + j) * kBN, bh);
+            tma_load_3d(kv_addr(s) + c * L::kChunkBytes, tm, bar(L::kKVFull + s), c * 64, jt * kBN, bh);
           ++kv_pos;
           return true;
         };
         for (int k = 0; ok; ++k) {
-          const int t = item_of(k, p);
-          if (t < 0) break;
-          int nk, n0, n1;
-          const Item it = decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, jb, nk, n0, n1);
+          if (!decode_unit<CAUSAL, SPLITK, PARTIAL, PAIR>(k, p, U)) break;
+          const int nk = U.nk;
           if (nk == 0) continue;  // empty split-KV range: nothing to load
           // Q tiles: wait until every S MMA of the previous item has read them.
           if (!(ok = wait_phase(bar(L::kQEmpty), (q_loads & 1) ^ 1, watch, 0))) break;
-          const int nq = (!SPLITK && n1 > 0) ? 2 : 1;
+          const int nq = (SPLITK ? U.nb > 0 : U.n1 > 0) ? 2 : 1;
           mbar_arrive_expect_tx(bar(L::kQFull), nq * L::kTileBytes);
-          for (int i = 0; i < nq; ++i)
+          for (int i = 0; i < nq; ++i) {
+            // two query tiles of one item, or (paired) a's query tile, then b's
+            const Item& qi = (SPLITK && i > 0) ? U.b : U.a;
+            const int row0 = SPLITK ? qi.mb * kBM : qi.mb * kItemRows + i * kBM;
             for (int c = 0; c < L::kChunks; ++c)
-              tma_load_3d(q_addr(i) + c * L::kChunkBytes, &p.tm_q, bar(L::kQFull), c * 64,
-                          it.mb * kItemRows + i * kBM, it.bh);
+              tma_load_3d(q_addr(i) + c * L::kChunkBytes, &p.tm_q, bar(L::kQFull), c * 64, row0, qi.bh);
+          }
           ++q_loads;
           // K/V in the MMA warp's consumption order:
           //   two query tiles, P in S's columns:   K0 V0 K1 V1 K2 ...
@@ -389,21 +487,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           //   split-K, P in S's columns:           K0 K1 V0 K2 V1 K3 V2 ...
           //   split-K, separate P:                 K0 K1 K2 K3 V0 V1 K4 K5 V2 V3 ...
           if (!SPLITK && !kSepP) {
-            for (int j = 0; j < nk && ok; ++j) ok = load_kv(&p.tm_k, j, it.bh) && load_kv(&p.tm_v, j, it.bh);
+            for (int j = 0; j < nk && ok; ++j) ok = load_kv(&p.tm_k, j) && load_kv(&p.tm_v, j);
           } else if (SPLITK && kSepP) {
-            ok = load_kv(&p.tm_k, 0, it.bh);
-            if (nk > 1) ok = ok && load_kv(&p.tm_k, 1, it.bh);
+            ok = load_kv(&p.tm_k, 0);
+            if (nk > 1) ok = ok && load_kv(&p.tm_k, 1);
             for (int t2 = 0; t2 < nk && ok; t2 += 2) {
-              if (t2 + 2 < nk) ok = ok && load_kv(&p.tm_k, t2 + 2, it.bh);
-              if (t2 + 3 < nk) ok = ok && load_kv(&p.tm_k, t2 + 3, it.bh);
-              ok = ok && load_kv(&p.tm_v, t2, it.bh);
-              if (t2 + 1 < nk) ok = ok && load_kv(&p.tm_v, t2 + 1, it.bh);
+              if (t2 + 2 < nk) ok = ok && load_kv(&p.tm_k, t2 + 2);
+              if (t2 + 3 < nk) ok = ok && load_kv(&p.tm_k, t2 + 3);
+              ok = ok && load_kv(&p.tm_v, t2);
+              if (t2 + 1 < nk) ok = ok && load_kv(&p.tm_v, t2 + 1);
             }
           } else {
-            ok = load_kv(&p.tm_k, 0, it.bh);
+            ok = load_kv(&p.tm_k, 0);
             for (int j = 0; j < nk && ok; ++j) {
-              if (j + 1 < nk) ok = load_kv(&p.tm_k, j + 1, it.bh);
-              ok = ok && load_kv(&p.tm_v, j, it.bh);
+              if (j + 1 < nk) ok = load_kv(&p.tm_k, j + 1);
+              ok = ok && load_kv(&p.tm_v, j);
             }
           }
         }
@@ -587,7 +685,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
         const uint32_t leader = elect_one_lane();
         constexpr uint32_t idesc_s = instr_desc_f16(BF16, kBM, kBN, false);
         constexpr uint32_t idesc_o = instr_desc_f16(BF16, kBM, D, true);
-        uint32_t kv_pos = 0, items = 0, merges = 0;
+        uint32_t kv_pos = 0, items = 0;
         uint32_t pcnt0 = 0, pcnt1 = 0;  // P hand-offs consumed per warpgroup
         bool ok = true;
         auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
@@ -645,6 +743,45 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           if (last) mma_commit_leader(bar(L::kOFull + w), leader);
           return true;
         };
+        // The same with the barrier to commit after the PV chosen by the caller (0: none), for
+        // the split-K form at D = 64, where a pair's b ends on a barrier of its own. The other
+        // paths keep the constant-barrier form: passing the barrier for every PV made the long
+        // D = 128 split-K chains 4-5% slower (c5, lc1).
+        auto issue_pv_to = [&](int w, uint32_t stage, bool accumulate, uint32_t done_bar) -> bool {
+          const uint32_t pc = w ? pcnt1 : pcnt0;
+          if (!wait(bar(L::kPFull + w), pc & 1, 5 + w)) return false;
+          if (w) ++pcnt1;
+          else ++pcnt0;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + TC::o(w);
+          const uint32_t a_tmem = tmem + TC::p(w);
+          const uint64_t b0 = v_desc + stage * kTileEnc;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts_leader(d_tmem, a_tmem + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_o,
+                          (accumulate || kk > 0) ? 1u : 0u, leader);
+          if (kSepP) mma_commit_leader(bar(L::kPVDone + w), leader);
+          if (done_bar != 0) mma_commit_leader(done_bar, leader);
+          return true;
+        };
+        // Split-K: warpgroup 1's O1 is overwritten by the first PV of each of its accumulations
+        // (an item's odd tiles; paired, b's tiles, then a's remaining ones), so whoever read the
+        // previous one must be done: warpgroup 0's merge (kO1Free) or, paired, warpgroup 1's
+        // own store (kO1Self). Both barriers complete once per such read, in order.
+        uint32_t merges = 0, selfs = 0;  // accumulations into O1 issued, by their reader
+        int o1_reader = 0;               // reader of the last one: 0 none, 1 merge, 2 own store
+        auto o1_begin = [&](bool own_b) -> bool {
+          if (o1_reader == 1 && !wait(bar(L::kO1Free), (merges - 1) & 1, 13)) return false;
+          if (o1_reader == 2 && !wait(bar(L::kO1Self), (selfs - 1) & 1, 13)) return false;
+          if (own_b) {
+            ++selfs;
+            o1_reader = 2;
+          } else {
+            ++merges;
+            o1_reader = 1;
+          }
+          return true;
+        };
         // Separate-P form: warpgroup w signals kSFree once per tile it processes (also for its
         // last tile of an item, which has no next S), so the waits name the completion they need:
         // the hand-back of tile u of the current item is completion tiles_w + u + 1, where tiles_w
@@ -660,14 +797,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
 
         if (p.force_stall) ok = wait(bar(L::kStall), 0, 12);  // runs out: exercises the abort path
         for (int k = 0; ok; ++k) {
-          const int t = item_of(k, p);
-          if (t < 0) break;
-          int jb, nk, n0, n1;
-          decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, jb, nk, n0, n1);
+          Unit U;
+          if (!decode_unit<CAUSAL, SPLITK, PARTIAL, PAIR>(k, p, U)) break;
+          const int nk = U.nk, n0 = U.n0, n1 = U.n1;
           if (nk == 0) continue;  // empty split-KV range
           s_left = SPLITK ? nk : n0 + n1;
           if (!(ok = wait(bar(L::kQFull), items & 1, 2))) break;
           uint32_t sk, sv;
+          // Split-K: Q tile read by warpgroup w's u-th S (paired: b's tile is the second one).
+          auto q_of = [&](int w, int u) -> int { return (PAIR && w == 1 && u < U.nb) ? 1 : 0; };
+          // Split-K PV of warpgroup w's u-th tile: opens an accumulation (and, for warpgroup 1,
+          // waits until O1 is free) or adds to it, and signals the end of one.
+          auto split_pv = [&](int w, int u, uint32_t stage) -> bool {
+            const bool b_end = PAIR && w == 1 && u == U.nb - 1;
+            const bool start = u == 0 || (PAIR && w == 1 && U.nb > 0 && u == U.nb);
+            if (w == 1 && start && !o1_begin(PAIR && u < U.nb)) return false;
+            const uint32_t done = b_end ? bar(L::kOFullB) : (u == (w ? n1 : n0) - 1 ? bar(L::kOFull + w) : 0u);
+            return issue_pv_to(w, stage, !start, done);
+          };
           if (kSepP && !SPLITK) {
             // Separate P: S_w(j+1) is issued as soon as warpgroup w has read S_w(j), before
             // PV_w(j), so the tensor core computes the next S while the softmax runs.
@@ -705,7 +852,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
             release(sk);
             if (nk > 1) {
               if (!(ok = next_slot(sk))) break;
-              issue_s(1, 0, sk);
+              issue_s(1, q_of(1, 0), sk);
               release(sk);
             }
             for (int t2 = 0; t2 < nk && ok; t2 += 2) {
@@ -713,7 +860,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
               for (int w = 0; w < 2; ++w) {
                 if (t2 + 2 + w < nk) {
                   if (!(ok = wait_s_free(w, t2 >> 1)) || !(ok = next_slot(sk))) break;
-                  issue_s(w, 0, sk);
+                  issue_s(w, q_of(w, (t2 >> 1) + 1), sk);
                   release(sk);
                 }
               }
@@ -722,15 +869,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
               for (int w = 0; w < 2; ++w) {
                 if (t2 + w < nk) {
                   if (!(ok = next_slot(sv))) break;
-                  // O1 is overwritten by the first PV of warpgroup 1: the previous item's merge
-                  // must have read it.
-                  if (w == 1 && t2 == 0 && merges > 0 && !(ok = wait(bar(L::kO1Free), (merges - 1) & 1, 13))) break;
-                  if (!(ok = issue_pv(w, sv, t2 > 0, t2 + w + 2 >= nk))) break;
+                  if (!(ok = split_pv(w, t2 >> 1, sv))) break;
                   release(sv);
                 }
               }
             }
-            if (ok && n1 > 0) ++merges;
           } else if (!SPLITK) {
             // Both query tiles against K0, then per K/V tile j: PV_w(j) and S_w(j+1), w = 0, 1.
             if (!(ok = next_slot(sk))) break;
@@ -757,7 +900,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
               if (k_next) release(sk);
             }
           } else {
-            // One query tile; K/V tile j belongs to warpgroup j & 1.
+            // One query tile; K/V tile j belongs to warpgroup j & 1 (P in S's columns: D = 128,
+            // never paired).
             //   S_0(K0), S_1(K1), then per j: PV_{j&1}(V_j), S_{j&1}(K_{j+2}).
             if (!(ok = next_slot(sk))) break;
             issue_s(0, 0, sk);
@@ -811,281 +955,298 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
-      const int t = item_of(k, p);
-      if (t < 0) break;
-      int jb, nk, n0, n1;
-      const Item it = decode_work<CAUSAL, SPLITK, PARTIAL>(t, p, jb, nk, n0, n1);
-      const int n_mine = wg == 0 ? n0 : n1;
-      const int qt = SPLITK ? it.mb : 2 * it.mb + wg;  // query tile index (its diagonal K tile)
-      const int row = qt * kBM + r;                     // query index within the sequence
+      Unit U;
+      if (!decode_unit<CAUSAL, SPLITK, PARTIAL, PAIR>(k, p, U)) break;
+      const int nk = U.nk, n1 = U.n1;
+      const int n_mine = wg == 0 ? U.n0 : U.n1;
       if (PARTIAL && nk == 0) {
         // Empty K/V range: the partial result has no key (lse = -inf; the merge skips it).
+        const int row = U.a.mb * kBM + r;
         if (wg == 0 && row < p.N)
-          p.lse_part[(static_cast<long long>(it.split) * p.BH + it.bh) * p.N + row] = -INFINITY;
+          p.lse_part[(static_cast<long long>(U.a.split) * p.BH + U.a.bh) * p.N + row] = -INFINITY;
         continue;
       }
       if (n_mine == 0) continue;
-      float m_used = -INFINITY;
-      float l_run = 0.f;
+      // One accumulation over this warpgroup's tiles, except for warpgroup 1 of a pair: b's
+      // tiles [0, nb), which it stores itself, then a's remaining tiles (if any).
+      const bool two_acc = PAIR && wg == 1 && U.nb > 0;
+      const int nseg = (two_acc && n1 > U.nb) ? 2 : 1;
+      for (int seg = 0; seg < nseg; ++seg) {
+        const bool own_b = two_acc && seg == 0;
+        const int u0 = seg == 0 ? 0 : U.nb;
+        const int u1 = own_b ? U.nb : n_mine;
+        const Item it = own_b ? U.b : U.a;
+        const int qt = SPLITK ? it.mb : 2 * it.mb + wg;  // query tile index (its diagonal K tile)
+        const int row = qt * kBM + r;                     // query index within the sequence
+        float m_used = -INFINITY;
+        float l_run = 0.f;
 
-      for (int jj = 0; jj < n_mine; ++jj) {
-        const int j = jb + (SPLITK ? 2 * jj + wg : jj);  // K/V tile index
-        bool w_ok = wait_phase(bar(L::kSFull + wg), scnt & 1, watch, 8 + wg);
-        if (!__all_sync(0xffffffffu, w_ok)) {
-          ok = false;
-          break;
-        }
-        ++scnt;
-        tc_fence_after();
-        uint32_t sr[kBN];
-        tmem_ld32x32b_x128(t_s, sr);
-        float* s = reinterpret_cast<float*>(sr);
-        if (kSepP) {
-          // S is in registers: hand its TMEM columns back so the next S can be computed.
-          tc_fence_before();
-          mbar_arrive(bar(L::kSFree + wg));
-        }
-        bool abort_now = false;
+        for (int jj = u0; jj < u1; ++jj) {
+          int j = jj;  // K/V tile index
+          if (SPLITK) {
+            bool from_b;
+            j = unit_tile<PAIR>(U, wg, jj, from_b);
+          }
+          bool w_ok = wait_phase(bar(L::kSFull + wg), scnt & 1, watch, 8 + wg);
+          if (!__all_sync(0xffffffffu, w_ok)) {
+            ok = false;
+            break;
+          }
+          ++scnt;
+          tc_fence_after();
+          uint32_t sr[kBN];
+          tmem_ld32x32b_x128(t_s, sr);
+          float* s = reinterpret_cast<float*>(sr);
+          if (kSepP) {
+            // S is in registers: hand its TMEM columns back so the next S can be computed.
+            tc_fence_before();
+            mbar_arrive(bar(L::kSFree + wg));
+          }
+          bool abort_now = false;
 
-        const int col0 = j * kBN;
-        const bool diag = CAUSAL && j == qt;
-        if (diag || col0 + kBN > p.N) {
-          int lim = p.N - 1 - col0;
-          if (diag) lim = min(lim, row - col0);
+          const int col0 = j * kBN;
+          const bool diag = CAUSAL && j == qt;
+          if (diag || col0 + kBN > p.N) {
+            int lim = p.N - 1 - col0;
+            if (diag) lim = min(lim, row - col0);
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (c > lim) s[c] = -INFINITY;
-        }
-        // p = 2^(s * scale * log2 e - m) for the 64 columns of half h, packed to fp16/bf16
-        // pairs and stored as P over the first half of this tile's TMEM columns (P column c
-        // holds elements 2c, 2c+1; S is already in registers). Returns the half's row sum;
-        // four partial sums keep the dependency chains short.
-        auto exp_half = [&](float m, int h) -> float {
-          const uint64_t sl2x2 = f2_pack(sl2, sl2);
-          const uint64_t negm2 = f2_pack(-m, -m);
-          uint64_t acc[4] = {0, 0, 0, 0};
-          uint32_t pk[kBN / 4];
-#pragma unroll
-          for (int i = 0; i < kBN / 4; ++i) {
-            const int c = h * (kBN / 4) + i;  // column pair
-            const uint64_t x2 = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm2);
-            float x0, x1;
-            f2_unpack(x2, x0, x1);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
-            acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-            pk[i] = pack2<BF16>(p0, p1);
+            for (int c = 0; c < kBN; ++c)
+              if (c > lim) s[c] = -INFINITY;
           }
-          if (kSepP && h == 0 && p_sent > 0) {
-            // P has columns of its own: the previous PV must have read them (and finished
-            // with O) before they are overwritten.
-            const bool pv_ok = wait_phase(bar(L::kPVDone + wg), (p_sent - 1) & 1, watch, 15);
-            if (!__all_sync(0xffffffffu, pv_ok)) abort_now = true;
-            tc_fence_after();
+          // p = 2^(s * scale * log2 e - m) for the 64 columns of half h, packed to fp16/bf16
+          // pairs and stored as P over the first half of this tile's TMEM columns (P column c
+          // holds elements 2c, 2c+1; S is already in registers). Returns the half's row sum;
+          // four partial sums keep the dependency chains short.
+          auto exp_half = [&](float m, int h) -> float {
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t negm2 = f2_pack(-m, -m);
+            uint64_t acc[4] = {0, 0, 0, 0};
+            uint32_t pk[kBN / 4];
+#pragma unroll
+            for (int i = 0; i < kBN / 4; ++i) {
+              const int c = h * (kBN / 4) + i;  // column pair
+              const uint64_t x2 = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, negm2);
+              float x0, x1;
+              f2_unpack(x2, x0, x1);
+              const float p0 = ex2_approx(x0);
+              const float p1 = ex2_approx(x1);
+              acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+              pk[i] = pack2<BF16>(p0, p1);
+            }
+            if (kSepP && h == 0 && p_sent > 0) {
+              // P has columns of its own: the previous PV must have read them (and finished
+              // with O) before they are overwritten.
+              const bool pv_ok = wait_phase(bar(L::kPVDone + wg), (p_sent - 1) & 1, watch, 15);
+              if (!__all_sync(0xffffffffu, pv_ok)) abort_now = true;
+              tc_fence_after();
+            }
+            tmem_st32x32b_x32(t_p + h * (kBN / 4), pk);
+            float a0, a1, b0, b1, c0, c1, d0, d1;
+            f2_unpack(acc[0], a0, a1);
+            f2_unpack(acc[1], b0, b1);
+            f2_unpack(acc[2], c0, c1);
+            f2_unpack(acc[3], d0, d1);
+            return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+          };
+          // Row max of the raw scores (scale > 0, so it commutes with the scaling), in eight
+          // independent chains of 3-input max.
+          auto row_max = [&]() -> float {
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+            for (int c = 16; c < kBN; c += 16)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
+            return fmaxf(fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5])), fmaxf(mx[6], mx[7]));
+          };
+          // Tile max first, then the exponentials against the running max m_used. m_used only
+          // moves when the tile raises it by more than the threshold (then O and l are rescaled).
+          const float x_max = row_max() * sl2;
+          float alpha = 1.f;
+          bool rescale = false;
+          if (jj == u0) {
+            m_used = x_max;
+          } else if (x_max > m_used + kRescaleLog2) {
+            alpha = ex2_approx(m_used - x_max);
+            m_used = x_max;
+            l_run *= alpha;
+            rescale = true;
           }
-          tmem_st32x32b_x32(t_p + h * (kBN / 4), pk);
-          float a0, a1, b0, b1, c0, c1, d0, d1;
-          f2_unpack(acc[0], a0, a1);
-          f2_unpack(acc[1], b0, b1);
-          f2_unpack(acc[2], c0, c1);
-          f2_unpack(acc[3], d0, d1);
-          return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
-        };
-        // Row max of the raw scores (scale > 0, so it commutes with the scaling), in eight
-        // independent chains of 3-input max.
-        auto row_max = [&]() -> float {
-          float mx[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-          for (int c = 16; c < kBN; c += 16)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], s[c + 2 * i], s[c + 2 * i + 1]);
-          return fmaxf(fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5])), fmaxf(mx[6], mx[7]));
-        };
-        // Tile max first, then the exponentials against the running max m_used. m_used only
-        // moves when the tile raises it by more than the threshold (then O and l are rescaled).
-        const float x_max = row_max() * sl2;
-        float alpha = 1.f;
-        bool rescale = false;
-        if (jj == 0) {
-          m_used = x_max;
-        } else if (x_max > m_used + kRescaleLog2) {
-          alpha = ex2_approx(m_used - x_max);
-          m_used = x_max;
-          l_run *= alpha;
-          rescale = true;
-        }
-        l_run += exp_half(m_used, 0) + exp_half(m_used, 1);
-        if (__any_sync(0xffffffffu, rescale)) {
-          // O row *= alpha (alpha = 1 for rows that keep their max). The previous PV of this
-          // warpgroup has completed: with P in S's columns this tile's S was issued after it;
-          // with separate P the kPVDone wait above covered it.
+          l_run += exp_half(m_used, 0) + exp_half(m_used, 1);
+          if (__any_sync(0xffffffffu, rescale)) {
+            // O row *= alpha (alpha = 1 for rows that keep their max). The previous PV of this
+            // warpgroup has completed: with P in S's columns this tile's S was issued after it;
+            // with separate P the kPVDone wait above covered it.
 #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_ld32x32b_x32(t_o + c, o);
+            for (int c = 0; c < D; c += 32) {
+              uint32_t o[32];
+              tmem_ld32x32b_x32(t_o + c, o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32x32b_x32(t_o + c, o);
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32x32b_x32(t_o + c, o);
+            }
           }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(L::kPFull + wg));
-        ++p_sent;
-        if (abort_now) {
-          ok = false;
-          break;
-        }
-      }
-      if (!ok) break;
-
-      if (SPLITK && wg == 1) {
-        // Hand (m, l) of the odd K/V tiles to warpgroup 0, which merges and stores. The
-        // previous hand-off must have been read first (warpgroup 0 signals kO1Free).
-        if (mcnt > 0) {
-          const bool f_ok = wait_phase(bar(L::kO1Free), (mcnt - 1) & 1, watch, 14);
-          if (!__all_sync(0xffffffffu, f_ok)) {
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(L::kPFull + wg));
+          ++p_sent;
+          if (abort_now) {
             ok = false;
             break;
           }
         }
-        ++mcnt;
-        stats_m[r] = m_used;
-        stats_l[r] = l_run;
-        mbar_arrive(bar(L::kStats));
-        continue;
-      }
+        if (!ok) break;
 
-      // ---------------- epilogue: O / l -> staging shared memory -> TMA store; lse
-      // Each warp stages and stores its own 32 rows, so no barrier spans warps.
-      bool e_ok = wait_phase(bar(L::kOFull + wg), ocnt & 1, watch, 10 + wg);
-      ++ocnt;
-      const bool merge = SPLITK && n1 > 0;
-      float a_self = 1.f, a_other = 0.f;
-      if (merge) {
-        // Partial results of the odd tiles: O1 in TMEM, (m1, l1) from warpgroup 1.
-        e_ok = e_ok && wait_phase(bar(L::kOFull + 1), o1cnt & 1, watch, 11);
-        e_ok = e_ok && wait_phase(bar(L::kStats), mcnt & 1, watch, 12);
-        ++o1cnt;
-        ++mcnt;
-      }
-      if (!__all_sync(0xffffffffu, e_ok)) {
-        ok = false;
-        break;
-      }
-      if (merge) {
-        const float m1 = stats_m[r], l1 = stats_l[r];
-        const float m = fmaxf(m_used, m1);
-        a_self = ex2_approx(m_used - m);
-        a_other = ex2_approx(m1 - m);
-        l_run = l_run * a_self + l1 * a_other;
-        m_used = m;
-      }
-      if (lane == 0) bulk_wait_group_read0();  // this warp's previous store has left the buffer
-      __syncwarp();
-      tc_fence_after();
-      const float inv_l = 1.0f / l_run;
-      const float c_self = a_self * inv_l, c_other = a_other * inv_l;
-      const uint32_t ob = o_addr(wg);
-      // Split-KV partial form: warp wq's fp32 boxes go to its quarter of the O staging tile of
-      // warpgroup 0, then to its quarter of warpgroup 1's (which stages nothing in this form).
-      auto part_box = [&](int b) -> uint32_t {
-        constexpr int kPerRegion = D / 64;  // 4 KB boxes per quarter tile
-        const uint32_t region = b < kPerRegion ? o_addr(0) : o_addr(1);
-        return region + wq * (L::kTileBytes / 4) + (b % kPerRegion) * 4096;
-      };
-      // Columns per step: 64 (one 128-byte swizzle chunk) at D = 64; 32 at D = 128, where the
-      // merge would otherwise hold two 64-column O rows at once.
-      constexpr int kEpi = (D == 64) ? 64 : 32;
-#pragma unroll 1
-      for (int c = 0; c < D; c += kEpi) {
-        uint32_t o[kEpi];
-        if (merge) {
-          uint32_t o1[kEpi];
-          if constexpr (kEpi == 64) tmem_ld32x32b_x64_pair(t_o + c, t_o1 + c, o, o1);
-          else tmem_ld32x32b_x32_pair(t_o + c, t_o1 + c, o, o1);
-#pragma unroll
-          for (int e = 0; e < kEpi; ++e)
-            o[e] = __float_as_uint(__uint_as_float(o[e]) * c_self + __uint_as_float(o1[e]) * c_other);
-        } else {
-          if constexpr (kEpi == 64) tmem_ld32x32b_x64(t_o + c, o);
-          else tmem_ld32x32b_x32(t_o + c, o);
-#pragma unroll
-          for (int e = 0; e < kEpi; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c_self);
+        if (SPLITK && wg == 1 && !own_b) {
+          // Hand (m, l) of its K/V tiles of the item to warpgroup 0, which merges and stores.
+          // The previous hand-off must have been read first (warpgroup 0 signals kO1Free).
+          if (mcnt > 0) {
+            const bool f_ok = wait_phase(bar(L::kO1Free), (mcnt - 1) & 1, watch, 14);
+            if (!__all_sync(0xffffffffu, f_ok)) {
+              ok = false;
+              break;
+            }
+          }
+          ++mcnt;
+          stats_m[r] = m_used;
+          stats_l[r] = l_run;
+          mbar_arrive(bar(L::kStats));
+          continue;
         }
-        if constexpr (PARTIAL) {
-          // fp32 partial rows: each warp stages its 32 rows as D/32 boxes of 32 rows x 32
-          // columns (128-byte swizzled rows, 4 KB each), then stores them with TMA.
+
+        // ---------------- epilogue: O / l -> staging shared memory -> TMA store; lse
+        // Each warp stages and stores its own 32 rows, so no barrier spans warps.
+        // (warpgroup 1 of a pair, for b: its own last-PV barrier, which only it waits on)
+        bool e_ok = wait_phase(bar(own_b ? L::kOFullB : L::kOFull + wg), ocnt & 1, watch, 10 + wg);
+        ++ocnt;
+        const bool merge = SPLITK && wg == 0 && n1 > U.nb;
+        float a_self = 1.f, a_other = 0.f;
+        if (merge) {
+          // Partial results of the odd tiles: O1 in TMEM, (m1, l1) from warpgroup 1.
+          e_ok = e_ok && wait_phase(bar(L::kOFull + 1), o1cnt & 1, watch, 11);
+          e_ok = e_ok && wait_phase(bar(L::kStats), mcnt & 1, watch, 12);
+          ++o1cnt;
+          ++mcnt;
+        }
+        if (!__all_sync(0xffffffffu, e_ok)) {
+          ok = false;
+          break;
+        }
+        if (merge) {
+          const float m1 = stats_m[r], l1 = stats_l[r];
+          const float m = fmaxf(m_used, m1);
+          a_self = ex2_approx(m_used - m);
+          a_other = ex2_approx(m1 - m);
+          l_run = l_run * a_self + l1 * a_other;
+          m_used = m;
+        }
+        if (lane == 0) bulk_wait_group_read0();  // this warp's previous store has left the buffer
+        __syncwarp();
+        tc_fence_after();
+        const float inv_l = 1.0f / l_run;
+        const float c_self = a_self * inv_l, c_other = a_other * inv_l;
+        const uint32_t ob = o_addr(wg);
+        // Split-KV partial form: warp wq's fp32 boxes go to its quarter of the O staging tile of
+        // warpgroup 0, then to its quarter of warpgroup 1's (which stages nothing in this form).
+        auto part_box = [&](int b) -> uint32_t {
+          constexpr int kPerRegion = D / 64;  // 4 KB boxes per quarter tile
+          const uint32_t region = b < kPerRegion ? o_addr(0) : o_addr(1);
+          return region + wq * (L::kTileBytes / 4) + (b % kPerRegion) * 4096;
+        };
+        // Columns per step: 64 (one 128-byte swizzle chunk) at D = 64; 32 at D = 128, where the
+        // merge would otherwise hold two 64-column O rows at once.
+        constexpr int kEpi = (D == 64) ? 64 : 32;
+#pragma unroll 1
+        for (int c = 0; c < D; c += kEpi) {
+          uint32_t o[kEpi];
+          if (merge) {
+            uint32_t o1[kEpi];
+            if constexpr (kEpi == 64) tmem_ld32x32b_x64_pair(t_o + c, t_o1 + c, o, o1);
+            else tmem_ld32x32b_x32_pair(t_o + c, t_o1 + c, o, o1);
 #pragma unroll
-          for (int u = 0; u < kEpi / 4; ++u) {
-            const int col = c + 4 * u;
-            const uint32_t addr = part_box(col >> 5) + lane * 128 + ((((col & 31) >> 2) ^ (lane & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o[4 * u + 0]),
-                         "r"(o[4 * u + 1]), "r"(o[4 * u + 2]), "r"(o[4 * u + 3])
+            for (int e = 0; e < kEpi; ++e)
+              o[e] = __float_as_uint(__uint_as_float(o[e]) * c_self + __uint_as_float(o1[e]) * c_other);
+          } else {
+            if constexpr (kEpi == 64) tmem_ld32x32b_x64(t_o + c, o);
+            else tmem_ld32x32b_x32(t_o + c, o);
+#pragma unroll
+            for (int e = 0; e < kEpi; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c_self);
+          }
+          if constexpr (PARTIAL) {
+            // fp32 partial rows: each warp stages its 32 rows as D/32 boxes of 32 rows x 32
+            // columns (128-byte swizzled rows, 4 KB each), then stores them with TMA.
+#pragma unroll
+            for (int u = 0; u < kEpi / 4; ++u) {
+              const int col = c + 4 * u;
+              const uint32_t addr = part_box(col >> 5) + lane * 128 + ((((col & 31) >> 2) ^ (lane & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o[4 * u + 0]),
+                           "r"(o[4 * u + 1]), "r"(o[4 * u + 2]), "r"(o[4 * u + 3])
+                           : "memory");
+            }
+            continue;
+          }
+          if constexpr (L::kOneChunkStaging) {
+            if (c > 0 && (c & 63) == 0) {
+              // Store the previous 64-column chunk; its reads must finish before the staging
+              // area is written again.
+              fence_proxy_async_smem();
+              __syncwarp();
+              const int row0 = qt * kBM + wq * 32;
+              if (lane == 0 && row0 < p.N) {
+                tma_store_3d(&p.tm_o, ob + wq * 32 * 128, c - 64, row0, it.bh);
+                bulk_commit_group();
+                bulk_wait_group_read0();
+              }
+              __syncwarp();
+            }
+          }
+          // 16-byte units (8 columns) of the 128-byte swizzled row of the 64-column chunk.
+          const uint32_t row_base = ob + (L::kOneChunkStaging ? 0 : (c >> 6) * L::kChunkBytes) + r * 128;
+#pragma unroll
+          for (int u = 0; u < kEpi / 8; ++u) {
+            const int unit = ((c & 63) >> 3) + u;
+            const uint32_t addr = row_base + ((unit ^ (r & 7)) << 4);
+            const uint32_t w0 = pack2<BF16>(__uint_as_float(o[8 * u + 0]), __uint_as_float(o[8 * u + 1]));
+            const uint32_t w1 = pack2<BF16>(__uint_as_float(o[8 * u + 2]), __uint_as_float(o[8 * u + 3]));
+            const uint32_t w2 = pack2<BF16>(__uint_as_float(o[8 * u + 4]), __uint_as_float(o[8 * u + 5]));
+            const uint32_t w3 = pack2<BF16>(__uint_as_float(o[8 * u + 6]), __uint_as_float(o[8 * u + 7]));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
                          : "memory");
+          }
+        }
+        tc_fence_before();
+        if (merge) mbar_arrive(bar(L::kO1Free));  // O1 and (m1, l1) consumed
+        if (own_b) mbar_arrive(bar(L::kO1Self));  // O1 read for b's store
+        if constexpr (PARTIAL) {
+          if (row < p.N)
+            p.lse_part[(static_cast<long long>(it.split) * p.BH + it.bh) * p.N + row] = (m_used + log2f(l_run)) * kLn2;
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int row0_warp = qt * kBM + wq * 32;
+          if (lane == 0 && row0_warp < p.N) {
+            for (int b = 0; b < D / 32; ++b)
+              tma_store_3d(&p.tm_op, part_box(b), b * 32, row0_warp, it.split * p.BH + it.bh);
+            bulk_commit_group();
           }
           continue;
         }
-        if constexpr (L::kOneChunkStaging) {
-          if (c > 0 && (c & 63) == 0) {
-            // Store the previous 64-column chunk; its reads must finish before the staging
-            // area is written again.
-            fence_proxy_async_smem();
-            __syncwarp();
-            const int row0 = qt * kBM + wq * 32;
-            if (lane == 0 && row0 < p.N) {
-              tma_store_3d(&p.tm_o, ob + wq * 32 * 128, c - 64, row0, it.bh);
-              bulk_commit_group();
-              bulk_wait_group_read0();
-            }
-            __syncwarp();
-          }
-        }
-        // 16-byte units (8 columns) of the 128-byte swizzled row of the 64-column chunk.
-        const uint32_t row_base = ob + (L::kOneChunkStaging ? 0 : (c >> 6) * L::kChunkBytes) + r * 128;
-#pragma unroll
-        for (int u = 0; u < kEpi / 8; ++u) {
-          const int unit = ((c & 63) >> 3) + u;
-          const uint32_t addr = row_base + ((unit ^ (r & 7)) << 4);
-          const uint32_t w0 = pack2<BF16>(__uint_as_float(o[8 * u + 0]), __uint_as_float(o[8 * u + 1]));
-          const uint32_t w1 = pack2<BF16>(__uint_as_float(o[8 * u + 2]), __uint_as_float(o[8 * u + 3]));
-          const uint32_t w2 = pack2<BF16>(__uint_as_float(o[8 * u + 4]), __uint_as_float(o[8 * u + 5]));
-          const uint32_t w3 = pack2<BF16>(__uint_as_float(o[8 * u + 6]), __uint_as_float(o[8 * u + 7]));
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
-                       : "memory");
-        }
-      }
-      tc_fence_before();
-      if (merge) mbar_arrive(bar(L::kO1Free));  // O1 and (m1, l1) consumed
-      if constexpr (PARTIAL) {
-        if (row < p.N)
-          p.lse_part[(static_cast<long long>(it.split) * p.BH + it.bh) * p.N + row] = (m_used + log2f(l_run)) * kLn2;
+        if (p.lse != nullptr && row < p.N)
+          p.lse[static_cast<long long>(it.bh) * p.N + row] = (m_used + log2f(l_run)) * kLn2;
         fence_proxy_async_smem();
         __syncwarp();
         const int row0_warp = qt * kBM + wq * 32;
-        if (lane == 0 && row0_warp < p.N) {
-          for (int b = 0; b < D / 32; ++b)
-            tma_store_3d(&p.tm_op, part_box(b), b * 32, row0_warp, it.split * p.BH + it.bh);
+        if (lane == 0 && row0_warp < p.N) {  // rows past N are clipped by the store; skip empty boxes
+          if constexpr (L::kOneChunkStaging) {
+            tma_store_3d(&p.tm_o, ob + wq * 32 * 128, D - 64, row0_warp, it.bh);
+          } else {
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_store_3d(&p.tm_o, ob + c * L::kChunkBytes + wq * 32 * 128, c * 64, row0_warp, it.bh);
+          }
           bulk_commit_group();
         }
-        continue;
       }
-      if (p.lse != nullptr && row < p.N)
-        p.lse[static_cast<long long>(it.bh) * p.N + row] = (m_used + log2f(l_run)) * kLn2;
-      fence_proxy_async_smem();
-      __syncwarp();
-      const int row0_warp = qt * kBM + wq * 32;
-      if (lane == 0 && row0_warp < p.N) {  // rows past N are clipped by the store; skip empty boxes
-        if constexpr (L::kOneChunkStaging) {
-          tma_store_3d(&p.tm_o, ob + wq * 32 * 128, D - 64, row0_warp, it.bh);
-        } else {
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_store_3d(&p.tm_o, ob + c * L::kChunkBytes + wq * 32 * 128, c * 64, row0_warp, it.bh);
-        }
-        bulk_commit_group();
-      }
+      if (!ok) break;
     }
     if (lane == 0) bulk_wait_group0();
     __syncwarp();

@@ -1,5 +1,5 @@
-// Kernel launcher template, explicitly instantiated in fa_inst_d64.cu, fa_inst_d128.cu and
-// fa_inst_partial.cu so that the kernel variants compile in parallel.
+// Kernel launcher template, explicitly instantiated in fa_inst_d64.cu, fa_inst_d128.cu,
+// fa_inst_partial.cu and fa_inst_pair.cu so that the kernel variants compile in parallel.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -10,10 +10,10 @@
 
 namespace fa {
 
-template <int D, bool BF16, bool CAUSAL, bool SPLITK, bool PARTIAL = false>
+template <int D, bool BF16, bool CAUSAL, bool SPLITK, bool PARTIAL = false, bool PAIR = false>
 cudaError_t launch_forward(const Params& p, int grid, cudaStream_t stream) {
-  using L = SmemLayout<D, SPLITK, !SPLITK>;
-  auto kernel = fa_fwd_kernel<D, BF16, CAUSAL, SPLITK, PARTIAL>;
+  using L = KernelLayout<D, SPLITK, PAIR>;
+  auto kernel = fa_fwd_kernel<D, BF16, CAUSAL, SPLITK, PARTIAL, PAIR>;
   // Opt in to the large dynamic shared-memory carve-out once per device.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -58,5 +58,7 @@ cudaError_t launch_forward_f32(const Params& p, int grid, int D, bool causal, cu
   EXT template cudaError_t launch_forward<D, BF16, CAUSAL, true, false>(const Params&, int, cudaStream_t);
 #define FA_DECLARE_LAUNCH_PARTIAL(EXT, D, BF16, CAUSAL) \
   EXT template cudaError_t launch_forward<D, BF16, CAUSAL, true, true>(const Params&, int, cudaStream_t);
+#define FA_DECLARE_LAUNCH_PAIR(EXT, D, BF16, CAUSAL) \
+  EXT template cudaError_t launch_forward<D, BF16, CAUSAL, true, false, true>(const Params&, int, cudaStream_t);
 
 }  // namespace fa

@@ -32,6 +32,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 FA_DECOMP_AUTO = 0
 FA_DECOMP_TWO_TILES = 1
 FA_DECOMP_SPLIT_KV = 2
+FA_DECOMP_SPLIT_KV_SERIAL = 3
 
 # Every symbol include/fa.h declares, with its ctypes signature.
 SIGNATURES = {
@@ -46,6 +47,7 @@ SIGNATURES = {
     "fa_set_decomposition": (ctypes.c_int, [ctypes.c_int]),
     "fa_debug_force_stall": (ctypes.c_int, [ctypes.c_int]),
     "fa_debug_work_schedule": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_int]),
+    "fa_debug_work_plan": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]),
     "fa_forward_splitkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
@@ -120,7 +122,7 @@ def set_watchdog_ns(ns: int) -> None:
 
 
 def set_decomposition(mode: int) -> None:
-    """Process-wide work decomposition (FA_DECOMP_AUTO / _TWO_TILES / _SPLIT_KV)."""
+    """Process-wide work decomposition (FA_DECOMP_AUTO / _TWO_TILES / _SPLIT_KV / _SPLIT_KV_SERIAL)."""
     _check(load_library().fa_set_decomposition(int(mode)))
 
 
@@ -355,3 +357,25 @@ def naive_forward(q, k, v, causal: bool = False, scale: float | None = None, wor
         raise FAError(rc, error_string(rc) + " (cublasStatus %d)" % load_library().fa_naive_last_library_error())
     _check(rc)
     return out, lse
+
+
+def debug_work_plan(B: int, H: int, N: int, D: int, causal: bool, dtype: int, num_sms: int):
+    """The work decomposition ``fa_forward`` would use for this shape on ``num_sms`` SMs (host
+    only): a dict with ``items``, ``single_tile``, ``paired``, ``dispatch`` and ``grid``, and for
+    paired launches ``units``, one tuple per CTA (item a, item b or -1, tiles of a, tiles of b,
+    tiles of warpgroup 0, tiles of warpgroup 1)."""
+    lib = load_library()
+    args = (int(B), int(H), int(N), int(D), int(bool(causal)), int(dtype), int(num_sms))
+    plan = (ctypes.c_int * 5)()
+    n = lib.fa_debug_work_plan(*args, ctypes.addressof(plan), None, 0)
+    if n < 0:
+        _check(n)
+    out = dict(zip(("items", "single_tile", "paired", "dispatch", "grid"), list(plan)))
+    out["single_tile"], out["paired"], out["dispatch"] = (bool(out[k]) for k in ("single_tile", "paired", "dispatch"))
+    out["units"] = None
+    if n > 0:
+        buf = (ctypes.c_int * n)()
+        _check(min(0, lib.fa_debug_work_plan(*args, ctypes.addressof(plan), ctypes.addressof(buf), n)))
+        vals = list(buf)
+        out["units"] = [tuple(vals[6 * c:6 * c + 6]) for c in range(n // 6)]
+    return out
