@@ -394,3 +394,152 @@ def test_o1_waits_are_implied_by_the_issue_order():
         m = type("M", (Dropped,), {"drop": ("O1Free", "O1Self")})([(6, 0), (5, 2), (7, 1), (4, 0)], 3, seed=seed)
         m.run()
         check_final(m)
+
+
+# ---- the same protocol with one MMA issuer per warpgroup (a form not built: the next step for
+# the paired form, whose warpgroup 1 then no longer holds up warpgroup 0's PVs). Both issuers
+# walk every ring position in the producer's order and release each (a commit where they used
+# it, a plain arrive where not); a stage is free once both released it, and Q once both issued
+# their last S. Each issuer has its own in-order tensor queue: a commit covers only the MMAs
+# of the warp that issued it.
+
+class CBar:
+    """A barrier that completes a phase after `count` arrivals."""
+
+    def __init__(self, name, count):
+        self.name, self.count, self.pend, self.done = name, count, 0, 0
+
+    def complete(self):  # one arrival
+        self.pend += 1
+        assert self.pend <= self.count, self.name
+        if self.pend == self.count:
+            self.pend = 0
+            self.done += 1
+
+
+class Dual(Model):
+    """The protocol with an MMA issuer per warpgroup."""
+
+    def __init__(self, units, stages, seed):
+        super().__init__(units, stages, seed)
+        for s in range(stages):
+            self.B[("KE", s)] = CBar(("KE", s), 2)
+        self.B["QE"] = CBar("QE", 2)
+        self.pipes = {0: [], 1: []}
+
+    def issuer(self, w):
+        pos = 0
+        merges = selfs = 0
+        reader = 0
+        pc = 0
+        tiles_w = 0
+        for k, (na, nb) in enumerate(self.units):
+            nk, n0, n1 = self.split(na, nb)
+            n_w = n1 if w else n0
+            while not self.ready("QF", k + 1):
+                yield
+            s_left = [n_w]
+            if n_w == 0:
+                self.B["QE"].complete()
+            pipe = self.pipes[w]
+            for kind, j in self.ring(nk):
+                s = pos % self.stages
+                while not self.ready(("KF", s), pos // self.stages + 1):
+                    yield
+                pos += 1
+                u, mine = j >> 1, (j & 1) == w
+                if not mine:
+                    self.B[("KE", s)].complete()  # plain arrive
+                    yield
+                    continue
+                if kind == "K":
+                    if u > 0:
+                        while not self.ready(("SFree", w), tiles_w + u):
+                            yield
+                    qb = 1 if (w == 1 and u < nb) else 0
+                    pipe.append(("S", (k, w, u, s, j, qb)))
+                    pipe.append(("commit", ("SF", w)))
+                    s_left[0] -= 1
+                    if s_left[0] == 0:
+                        pipe.append(("commit", "QE"))
+                    pipe.append(("commit", ("KE", s)))
+                else:
+                    start = u == 0 or (w == 1 and nb > 0 and u == nb)
+                    if w == 1 and start:
+                        if reader == 1:
+                            while not self.ready("O1Free", merges):
+                                yield
+                        if reader == 2:
+                            while not self.ready("O1Self", selfs):
+                                yield
+                        if u < nb:
+                            selfs, reader = selfs + 1, 2
+                        else:
+                            merges, reader = merges + 1, 1
+                    while not self.ready(("PF", w), pc + 1):
+                        yield
+                    pc += 1
+                    tag = (k, w, "b" if (w == 1 and u < nb) else "a")
+                    pipe.append(("PV", (k, w, u, s, j, not start, tag)))
+                    pipe.append(("commit", ("PVD", w)))
+                    if w == 1 and u == nb - 1:
+                        pipe.append(("commit", "OFB"))
+                    elif u == n_w - 1:
+                        pipe.append(("commit", ("OF", w)))
+                    pipe.append(("commit", ("KE", s)))
+                yield
+            tiles_w += n_w
+
+    def tensor_pipe_w(self, w):
+        while True:
+            self.pipe = self.pipes[w]
+            if not self.pipe:
+                yield
+                continue
+            g = super().tensor_pipe()
+            next(g)  # executes one op of self.pipe
+            yield
+
+    def run(self, max_steps=600000):
+        roles = {"producer": self.producer(), "mma0": self.issuer(0), "mma1": self.issuer(1),
+                 "wg0": self.softmax(0), "wg1": self.softmax(1)}
+        engines = [self.tensor_pipe_w(0), self.tensor_pipe_w(1), self.copy_engine()]
+        live = dict(roles)
+        for _ in range(max_steps):
+            if not live and not self.pipes[0] and not self.pipes[1] and not self.tma:
+                return
+            g = self.rnd.choice(list(live.values()) + engines)
+            try:
+                next(g)
+            except StopIteration:
+                live = {n: r for n, r in live.items() if r is not g}
+        raise AssertionError("deadlock: %s" % sorted(live))
+
+
+
+
+def test_two_issuer_form_of_the_protocol():
+    rnd = random.Random(7)
+    for stages in (2, 3, 8):
+        for _ in range(120):
+            m = Dual(random_units(rnd, 0.7), stages, seed=rnd.randrange(1 << 30))
+            m.run()
+            check_final(m)
+
+
+def test_two_issuer_form_needs_the_o1_waits():
+    class NoO1(Dual):
+        def ready(self, name, c):
+            if name in ("O1Free", "O1Self"):
+                return True
+            return super().ready(name, c)
+
+    failures = 0
+    for seed in range(300):
+        try:
+            m = NoO1([(6, 0), (5, 2), (7, 1)], 8, seed=seed)
+            m.run()
+            check_final(m)
+        except AssertionError:
+            failures += 1
+    assert failures > 0
