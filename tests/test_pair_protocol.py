@@ -9,7 +9,9 @@ and the copy engine (loads land in any order). Random interleavings of many unit
 must finish (no deadlock), every parity wait must find its barrier at the phase it waits for
 or the one before (never two behind, never past it), and every buffer must hold what its
 reader expects: the ring slot's tile, the Q tile of the query tile, the S and P of the tile,
-and each accumulator's tiles, never overwritten before its reader is done.
+and each accumulator's tiles, never overwritten before its reader is done; and when a
+warpgroup writes a tile's P (where the in-place O rescale runs), every earlier PV of its
+accumulation has completed.
 
 A unit is (na, nb): one query tile with na K/V tiles (nb = 0: unpaired, tiles alternate
 between the warpgroups) or a pair, where warpgroup 0 takes a's first ceil((na + nb) / 2)
@@ -207,6 +209,12 @@ class Model:
                     if p_sent > 0:
                         while not self.ready(("PVD", w), p_sent):
                             yield
+                    if u > u0:
+                        # the in-place O rescale may run here: every earlier PV of the
+                        # accumulation has completed
+                        o = self.O[w]
+                        tag = (k, w, "b" if own_b else "a")
+                        assert o is not None and o["tag"] == tag and o["n"] == u - u0, ("rescale", o, tag, u)
                     assert self.P[w] is None or self.P[w][0] == "used", ("P overwritten", self.P[w], (k, w, u))
                     self.P[w] = ("P", k, w, u)
                     self.B[("PF", w)].complete()
