@@ -6,7 +6,9 @@ covered by the split-K model at D = 64 (test_pair_protocol.py).
 * two query tiles per item, D = 64: an MMA issuer per warpgroup, separate P columns, both
   issuers walking every ring position and releasing each (a stage is free once both did);
 * one query tile per item, D = 128: one issuer, P over S's columns, tiles alternating between
-  the warpgroups and warpgroup 0 merging warpgroup 1's part.
+  the warpgroups and warpgroup 0 merging warpgroup 1's part;
+* the fp32-I/O kernel: separate K and V rings, V transposer warps filling transposed-V
+  buffers for the PV, and Q copied into TMEM by the MMA warp before the item's S products.
 
 Each model follows the kernel's issue order, ring order and waits. Over random item sequences
 and interleavings (copies land in any order; each issuer's tensor queue runs in its order) every
@@ -580,3 +582,194 @@ def test_split_k_d128_o1_wait_is_implied_by_the_issue_order():
     M = type("M", (_Drop, SplitKD128), {"drop": ("O1Free",)})
     for seed in range(150):
         M([4, 5, 3, 6], 3, seed=seed).run()
+
+
+# ---------------------------------------------------------------- fp32 I/O kernel
+class SplitKF32(Base):
+    """The fp32 kernel: one query tile per item, 64-key tiles alternating between the
+    warpgroups; separate K and V rings; two transposer warps copy each V tile into a
+    transposed buffer (Vt) that the PV reads; Q is copied from its shared-memory tile into TMEM
+    by the MMA warp (in issue order, after the previous item's last S) and S reads it there."""
+
+    sep_p = False
+
+    def __init__(self, items, stages, seed):
+        self.kst, self.vst, self.nvt = stages
+        super().__init__(items, self.kst, seed)
+        for s in range(self.vst):
+            self.B[("VF", s)], self.B[("VE", s)] = Bar(("VF", s)), Bar(("VE", s))
+        for b in range(self.nvt):
+            self.B[("VtF", b)], self.B[("VtE", b)] = Bar(("VtF", b)), Bar(("VtE", b))
+        self.vslot, self.vt = {}, {}
+        self.q_tmem = None
+
+    def roles(self):
+        return {"producer": self.producer(), "mma": self.mma(), "tr": self.transposer(),
+                "wg0": self.softmax(0), "wg1": self.softmax(1)}
+
+    def producer(self):
+        kpos = vpos = 0
+        for k, nk in enumerate(self.items):
+            while not (k == 0 or self.ready("QE", k)):
+                yield
+            self.q_pending = 1
+            self.load("QF", ("q", 0), (k, 0))
+            yield
+            order = [("K", 0)]
+            for j in range(nk):
+                if j + 1 < nk:
+                    order.append(("K", j + 1))
+                order.append(("V", j))
+            for kind, j in order:
+                if kind == "K":
+                    s = kpos % self.kst
+                    while not (kpos < self.kst or self.ready(("KE", s), kpos // self.kst)):
+                        yield
+                    self.load(("KF", s), ("slot", s), (k, "K", j))
+                    kpos += 1
+                else:
+                    s = vpos % self.vst
+                    while not (vpos < self.vst or self.ready(("VE", s), vpos // self.vst)):
+                        yield
+                    self.load(("VF", s), ("vslot", s), (k, "V", j))
+                    vpos += 1
+                yield
+
+    def copy_engine(self):
+        while True:
+            if self.tma:
+                bar, (kind, idx), val = self.tma.pop(self.rnd.randrange(len(self.tma)))
+                if kind == "q":
+                    self.q[idx] = val
+                    self.q_pending -= 1
+                    if self.q_pending == 0:
+                        self.B[bar].arrive()
+                else:
+                    (self.vslot if kind == "vslot" else self.slot)[idx] = val
+                    self.B[bar].arrive()
+            yield
+
+    def transposer(self):
+        vpos = vtc = 0
+        for k, nk in enumerate(self.items):
+            for j in range(nk):
+                s, b = vpos % self.vst, vtc % self.nvt
+                while not self.ready(("VF", s), vpos // self.vst + 1):
+                    yield
+                while not (vtc < self.nvt or self.ready(("VtE", b), vtc // self.nvt)):
+                    yield
+                vpos += 1
+                vtc += 1
+                assert self.vslot.get(s) == (k, "V", j), ("V slot", self.vslot.get(s), (k, j))
+                assert self.vt.get(b, ("free",))[0] in ("free", "used"), ("Vt overwritten", self.vt.get(b))
+                yield
+                self.vt[b] = ("Vt", k, j)
+                self.B[("VE", s)].arrive()
+                self.B[("VtF", b)].arrive()
+                yield
+
+    def tensor(self, i):
+        while True:
+            qu = self.queues[i]
+            if qu and qu[0][0] == "CPQ":
+                _, k = qu.pop(0)
+                assert self.q.get(0) == (k, 0), ("Q tile", self.q.get(0), k)
+                self.q_tmem = k
+            elif qu and qu[0][0] == "PVT":
+                _, (k, w, u, b, j, acc) = qu.pop(0)
+                assert self.vt.get(b) == ("Vt", k, j), ("Vt", self.vt.get(b), (k, j))
+                self.vt[b] = ("used",)
+                self.slot[("vt", b)] = (k, "V", j)
+                self.exec_pv(k, w, u, ("vt", b), j, acc, (k, w))
+            elif qu and qu[0][0] == "SQ":
+                _, (k, w, u, s, j) = qu.pop(0)
+                assert self.q_tmem == k, ("Q in TMEM", self.q_tmem, k)
+                self.q[("tmem",)] = (k, 0)
+                self.exec_s(k, w, u, s, j, ("tmem",), (k, 0))
+            elif qu:
+                op, x = qu.pop(0)
+                assert op == "commit", op
+                self.B[x].arrive()
+            yield
+
+    def mma(self):
+        kpos = vtc = 0
+        pc = [0, 0]
+        merges = 0
+        qu = self.queues[0]
+        for k, nk in enumerate(self.items):
+            n1 = nk // 2
+            while not self.ready("QF", k + 1):
+                yield
+            qu.append(("CPQ", k))
+            qu.append(("commit", "QE"))
+
+            def take_k():
+                nonlocal kpos
+                s, c = kpos % self.kst, kpos // self.kst + 1
+                kpos += 1
+                return s, c
+
+            def issue_s(w, u, s, j):
+                qu.append(("SQ", (k, w, u, s, j)))
+                qu.append(("commit", ("SF", w)))
+                qu.append(("commit", ("KE", s)))
+
+            for j in range(min(nk, 2)):
+                s, c = take_k()
+                while not self.ready(("KF", s), c):
+                    yield
+                issue_s(j, 0, s, j)
+                yield
+            for j in range(nk):
+                w, u = j & 1, j >> 1
+                b, c = vtc % self.nvt, vtc // self.nvt + 1
+                while not self.ready(("VtF", b), c):
+                    yield
+                vtc += 1
+                if j == 1 and merges > 0:
+                    while not self.ready("O1Free", merges):
+                        yield
+                while not self.ready(("PF", w), pc[w] + 1):
+                    yield
+                pc[w] += 1
+                qu.append(("PVT", (k, w, u, b, j, j >= 2)))
+                qu.append(("commit", ("VtE", b)))
+                if j + 2 >= nk:
+                    qu.append(("commit", ("OF", w)))
+                yield
+                if j + 2 < nk:
+                    s, c = take_k()
+                    while not self.ready(("KF", s), c):
+                        yield
+                    issue_s(w, u + 1, s, j + 2)
+                    yield
+            if n1 > 0:
+                merges += 1
+
+    softmax = SplitKD128.softmax
+
+
+@pytest.mark.parametrize("stages", [(4, 2, 2), (2, 1, 1), (3, 2, 3), (2, 2, 1)])
+def test_fp32_kernel(stages):
+    rnd = random.Random(80 + sum(stages))
+    for _ in range(120):
+        items = [rnd.randint(1, 11) for _ in range(rnd.randint(1, 4))]
+        SplitKF32(items, stages, seed=rnd.randrange(1 << 30)).run()
+
+
+@pytest.mark.parametrize("drop,items", [
+    (("VtE", 0), [6, 5]),      # a transposed buffer rewritten before its PV read it
+    (("VE", 0), [6]),          # a V stage refilled before the transposers read it
+    (("VtF", 1), [5]),         # PV before its transposed V was written
+    ("QE", [1, 4]),            # the next Q tile loaded before the copy into TMEM read it
+])
+def test_fp32_model_catches_each_missing_wait(drop, items):
+    M = type("M", (_Drop, SplitKF32), {"drop": (drop,)})
+    failures = 0
+    for seed in range(300):
+        try:
+            M(items, (4, 2, 2), seed=seed).run()
+        except AssertionError:
+            failures += 1
+    assert failures > 0, drop
