@@ -1,10 +1,9 @@
 """GPU parity of the fp32-I/O forward (tf32 tensor-core products) against the fp64 oracle.
 
-Tolerance, from the arithmetic: the tensor core reads the fp32 operands Q, K, V as tf32 (the
-low 13 mantissa bits dropped, a relative change below 2^-10 per element), P is rounded to
-tf32, and everything else is fp32. Exact attention on inputs truncated that way differs from
-exact attention on the fp32 inputs by at most 2.4e-3 in O and lse on N(0,1) data of these
-shapes (computed with the oracle on the CPU); the tolerance is twice that: 5e-3 for both.
+Tolerance 5e-3 for O and lse, from the arithmetic (derived and pinned on the CPU in
+tests/test_f32_tolerance.py): the tensor core reads the fp32 operands Q, K, V as tf32 (the
+low 13 mantissa bits dropped), which moves exact attention by at most 3.5e-3 on these
+shapes; the kernel's rounding of P to tf32 adds at most 5e-4; the rest is fp32 arithmetic.
 """
 
 from __future__ import annotations
