@@ -28,6 +28,26 @@ def run_cuda(q, k, v, causal, scale, lse=True):
     return o64, l64
 
 
+def ulp(x, dtype):
+    """Unit in the last place of the I/O type at |x| (fp16: 10 fraction bits, bf16: 7)."""
+    frac_bits, min_exp = {"fp16": (10, -14), "bf16": (7, -126)}[dtype]
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** min_exp)))
+    return 2.0 ** (e - frac_bits)
+
+
+def worst_element(o, lse, ro, rl, dtype):
+    """Where the largest O error is, its size in output ulps, and the largest lse error."""
+    err_o = np.abs(o - ro)
+    i = np.unravel_index(np.argmax(err_o), err_o.shape)
+    rep = {"o_max_abs": float(err_o[i]), "o_at": tuple(int(x) for x in i), "o_want": float(ro[i]),
+           "o_got": float(o[i]), "o_err_ulps": float(err_o[i] / ulp(ro[i], dtype))}
+    if lse is not None:
+        err_l = np.abs(lse - rl)
+        j = np.unravel_index(np.argmax(err_l), err_l.shape)
+        rep.update(lse_max_abs=float(err_l[j]), lse_at=tuple(int(x) for x in j))
+    return rep
+
+
 def assert_close(o, lse, ro, rl, dtype, what=""):
     assert np.isfinite(o).all(), "non-finite O " + what
     err_o = np.abs(o - ro)
@@ -81,41 +101,20 @@ def test_workload_both_decompositions(name, decomposition):
     assert_close(o, lse, ro, rl, w.dtype, name + " " + decomposition)
 
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c3c", "p2s512", "p2s1024"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c3c", "c4", "c5", "p2s512", "p2s1024"])
 def test_workload_full_oracle(name):
-    """Every output element of the smaller workloads against the oracle."""
+    """Every output element of each workload against the oracle, the full-size ones included.
+
+    c5 (Q, K scaled by 4) is the long-sequence case where exp(m_old - m_new) underflows and
+    the kernel's deferred rescale acts; c4 is the batched bf16 causal prefill. The oracle
+    takes a few seconds (c4) to about twenty (c5) on 16 host cores. The worst element, its
+    error in output ulps and the worst lse error are printed (pytest -rP shows them)."""
     w = workloads.WORKLOADS[name]
     q, k, v = workloads.make_qkv(w)
     o, lse = run_cuda(q, k, v, w.causal, w.scale)
     ro, rl = oracle.attention(q, k, v, w.scale, w.causal)
+    print("parity %s: %r" % (name, worst_element(o, lse, ro, rl, w.dtype)))
     assert_close(o, lse, ro, rl, w.dtype, name)
-
-
-def sample_rows(w, n_heads=6, seed=0):
-    """(bh, i) pairs: tile edges, the first and last rows, and random rows of a few heads."""
-    rng = np.random.default_rng(seed)
-    BH, N = w.B * w.H, w.N
-    heads = sorted(set([0, BH - 1] + list(rng.integers(0, BH, size=n_heads))))
-    fixed = [0, 1, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1]
-    rows = []
-    for bh in heads:
-        idx = set(i for i in fixed if 0 <= i < N) | set(rng.integers(0, N, size=24).tolist())
-        rows += [(bh, i) for i in sorted(idx)]
-    return np.array(rows, dtype=np.int64)
-
-
-@pytest.mark.parametrize("name", ["c4", "c5"])
-def test_workload_sampled_rows(name):
-    """Full-size workloads: every output is finite; sampled rows match the oracle."""
-    w = workloads.WORKLOADS[name]
-    q, k, v = workloads.make_qkv(w)
-    o, lse = run_cuda(q, k, v, w.causal, w.scale)
-    assert np.isfinite(o).all() and np.isfinite(lse).all()
-    rows = sample_rows(w)
-    ro, rl = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
-    o_s = o.reshape(-1, w.N, w.D)[rows[:, 0], rows[:, 1]]
-    l_s = lse.reshape(-1, w.N)[rows[:, 0], rows[:, 1]]
-    assert_close(o_s, l_s, ro, rl, w.dtype, name)
 
 
 def test_lse_optional():
