@@ -79,9 +79,18 @@ enum fa_status {
  * for a failed launch and device-side timeouts, which fa_check_device_status() reports.
  * Thread-safe; one-time per-device setup runs on first use. Causal problems with more than
  * two waves of work items run on a persistent grid from a per-shape work table. The first
- * call of such a shape builds the table on the host and copies it synchronously into the
- * library's module memory (a few KB, no allocation), so it belongs outside stream capture.
- * A call captured first runs correctly without the table, with one CTA per work item.
+ * call of such a shape builds the table on the host and copies it into the library's module
+ * memory (a few KB, no allocation) with cudaMemcpyAsync on `stream`, then records an event;
+ * until that event is seen complete, later calls of the shape on any stream first make their
+ * stream wait on it. A call that would need the table while its stream is being captured (the
+ * shape's first call, or one whose stream cannot wait yet) runs correctly without it, with one
+ * CTA per work item; so does a call when the table pool (4 MB per device, kept for the life of
+ * the process) is full. fa_schedule_pool_status reports both.
+ *
+ * Device addresses in module memory (status word, work tables, the no-alloc scratch) and the
+ * per-thread launch parameters are cached for the life of the process: after
+ * cudaDeviceReset, or any other destruction of the primary context, the library must not be
+ * used again in the same process.
  */
 FA_API int fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
                float scale, int causal, int dtype, void* stream);
@@ -136,9 +145,11 @@ FA_API int fa_forward_splitkv(const void* q, const void* k, const void* v, void*
  * This entry point is an engineering convenience; the pages have no counterpart to it.
  *
  *   arguments   as fa_forward_splitkv, minus workspace and workspace_bytes.
- *   limit       the split count used (given, or chosen when num_splits is 0) must need at most
- *               32 MiB, i.e. fa_splitkv_workspace_bytes(B, H, N, D, splits) <= 33554432;
- *               otherwise FA_ERR_SCRATCH and nothing is enqueued. One split needs no scratch.
+ *   limit       a given split count must need at most 32 MiB, i.e.
+ *               fa_splitkv_workspace_bytes(B, H, N, D, splits) <= 33554432; otherwise
+ *               FA_ERR_SCRATCH and nothing is enqueued. With num_splits 0 the count is
+ *               fa_splitkv_num_splits's choice lowered, if needed, to the largest that fits
+ *               (down to one split, which needs no scratch), so it never fails for size.
  *   zeroing     nothing in the scratch has to start at zero; every partial that the merge
  *               reads is written by the same call first.
  *   setup       the first call on a device does one-time setup (the device checks of
@@ -298,6 +309,19 @@ FA_API int fa_debug_work_schedule(int B, int H, int N, int D, int causal, int dt
  */
 FA_API int fa_debug_work_plan(int B, int H, int N, int D, int causal, int dtype, int num_sms, int* plan, int* units,
                               int capacity);
+
+/*
+ * The per-device pool of work tables that causal multi-wave launches use (fa_forward). Host
+ * only; the one CUDA call is cudaGetDevice (for used_bytes).
+ *   used_bytes, capacity_bytes  (either may be NULL) bytes of the current device's 4 MB pool
+ *                               in use and in total;
+ *   fallbacks                   (may be NULL) launches in this process, on any device, that
+ *                               needed a table but ran without one (one CTA per work item:
+ *                               the same result, slower): the pool was full, or the stream
+ *                               was being captured before the table's copy was known complete.
+ * Returns FA_OK or FA_ERR_CUDA.
+ */
+FA_API int fa_schedule_pool_status(size_t* used_bytes, size_t* capacity_bytes, unsigned long long* fallbacks);
 
 /* The cudaError_t value behind the most recent FA_ERR_CUDA returned on this host thread. */
 FA_API int fa_last_cuda_error(void);

@@ -69,3 +69,27 @@ def test_first_call_inside_graph_capture_then_scheduled_replay():
     for o, l in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
     check_heads(w, q.cpu(), k.cpu(), v.cpu(), outs[0][0], outs[0][1], heads=[0, 23, 47])
+
+
+def test_first_call_on_a_side_stream_then_another_stream():
+    # A shape no other test uses: its first call copies the work table asynchronously on a
+    # non-blocking side stream; a second call of the same shape, issued right away on another
+    # non-blocking stream (no host synchronisation in between), must wait for that copy.
+    w = workloads.Workload("async", 1, 56, 1408, 64, "fp16", True, seed=5150)
+    q, k, v = (x.cuda() for x in workloads.make_qkv(w))
+    torch.cuda.synchronize()
+    used0, cap, fb0 = fa.schedule_pool_status()
+    s1 = torch.cuda.Stream()
+    s2 = torch.cuda.Stream()
+    with torch.cuda.stream(s1):
+        o1, l1 = fa.forward(q, k, v, causal=True, scale=w.scale)
+    with torch.cuda.stream(s2):
+        o2, l2 = fa.forward(q, k, v, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    used1, cap1, fb1 = fa.schedule_pool_status()
+    assert cap1 == cap == 4 << 20
+    assert used1 > used0, "the shape's work table was not made"
+    assert fb1 == fb0, "a launch ran without its work table"
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    check_heads(w, q.cpu(), k.cpu(), v.cpu(), o1, l1, heads=[0, 27, 55])

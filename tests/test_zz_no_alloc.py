@@ -53,3 +53,22 @@ def test_one_split_causal_multiwave_matches_fa_forward():
     torch.cuda.synchronize()
     fa.check_device_status()
     assert torch.equal(a, r) and torch.equal(la, lr)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,H,N,D,causal", [(1, 1, 16384, 128, True), (1, 1, 65536, 64, True),
+                                            (1, 1, 16384, 128, False)])
+def test_automatic_split_count_fits_the_scratch(B, H, N, D, causal):
+    # num_splits = 0: the cost model's choice, lowered to the largest count whose partials fit
+    # the 32 MiB scratch; never FA_ERR_SCRATCH. Same result as the workspace entry point with
+    # that count.
+    w = workloads.Workload("auto", B, H, N, D, "fp16", causal, seed=77 + N)
+    q, k, v = (x.cuda() for x in workloads.make_qkv(w))
+    S = fa.splitkv_num_splits(B, H, N, D, causal)
+    while S > 1 and fa.splitkv_workspace_bytes(B, H, N, D, S) > fa.NOALLOC_SCRATCH_BYTES:
+        S -= 1
+    a, la = fa.forward_splitkv_noalloc(q, k, v, causal=causal, scale=w.scale, num_splits=0)
+    r, lr = fa.forward_splitkv(q, k, v, causal=causal, scale=w.scale, num_splits=S)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    assert torch.equal(a, r) and torch.equal(la, lr)

@@ -163,6 +163,8 @@ struct LaunchKey {
   size_t workspace_bytes;
   bool operator==(const LaunchKey& o) const { return std::memcmp(this, &o, sizeof(LaunchKey)) == 0; }
 };
+struct ScheduleEntry;
+bool schedule_ready(ScheduleEntry& e, cudaStream_t s);
 struct LaunchEntry {
   LaunchKey key;
   Params params;
@@ -175,6 +177,7 @@ struct LaunchEntry {
   float* lse;
   long long rows;  // BH * N
   int num_sms;
+  ScheduleEntry* sched;  // the work table the params point to, or nullptr
   bool valid;
 };
 constexpr int kCacheSize = 4;
@@ -317,13 +320,26 @@ WorkPlan plan_work(Params& p, long long BH, int N, int D, bool causal, bool f32,
 // persistent CTA then prefetches the next item's Q and K/V during the current one, which the
 // per-item launch cannot. The device copies live in a fixed pool of module memory (4 MB per
 // device, a few KB per shape) for the process lifetime; shapes past its end launch one CTA per
-// item.
+// item (counted in g_schedule_fallbacks, reported by fa_schedule_pool_status).
+//
+// The first call of a shape copies its table with cudaMemcpyAsync on that call's stream (the
+// host table stays alive in the entry, as the copy's source) and records an event after the
+// copy. Until that event has been seen complete, every launch that uses the table first makes
+// its own stream wait on the event, so a launch on another stream cannot read the table early.
+// A launch under stream capture that would need such a wait runs without the table instead.
 struct ScheduleKey {
   int dev, BH, N, causal, splitk, f32, section, num_mb, num_items, grid;
   bool operator<(const ScheduleKey& o) const { return std::memcmp(this, &o, sizeof(ScheduleKey)) < 0; }
 };
+struct ScheduleEntry {
+  int* table = nullptr;          // device copy in the pool
+  std::vector<int> host;         // source of the asynchronous copy, kept for the process lifetime
+  cudaEvent_t copied = nullptr;  // recorded on the first caller's stream after the copy
+  std::atomic<bool> done{false}; // the copy is known to be complete
+};
 std::mutex g_schedule_mutex;
-std::map<ScheduleKey, int*> g_schedules;
+std::map<ScheduleKey, ScheduleEntry> g_schedules;
+std::atomic<unsigned long long> g_schedule_fallbacks{0};
 constexpr double kScheduleItemOverhead = 1.0;
 struct SchedulePool {
   int* base = nullptr;  // g_schedule_pool on this device
@@ -365,10 +381,44 @@ std::vector<int> build_schedule(const Params& p, bool causal, bool splitk, bool 
   return out;
 }
 
-// The device copy of the schedule for this shape, made on first use by a synchronous copy into
-// the pool (nullptr while the stream is being captured into a graph, when the pool is full or
-// when the copy fails: the caller then launches one CTA per item).
-const int* get_schedule(int dev, const Params& p, bool causal, bool splitk, bool f32, int grid, cudaStream_t s) {
+bool stream_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return true;  // unknown: treat as capturing (no copies, no waits)
+  }
+  return cap != cudaStreamCaptureStatusNone;
+}
+
+// Makes `s` ordered after the copy of the entry's table. False when it cannot (the stream is
+// being captured and the copy is not known to be complete, or a CUDA call failed): the caller
+// then launches without the table.
+bool schedule_ready(ScheduleEntry& e, cudaStream_t s) {
+  if (e.done.load(std::memory_order_acquire)) return true;
+  std::lock_guard<std::mutex> lock(g_schedule_mutex);
+  if (e.done.load(std::memory_order_relaxed)) return true;
+  if (stream_capturing(s)) return false;
+  const cudaError_t q = cudaEventQuery(e.copied);
+  if (q == cudaSuccess) {
+    e.done.store(true, std::memory_order_release);
+    return true;
+  }
+  if (q != cudaErrorNotReady) {
+    cudaGetLastError();
+    return false;
+  }
+  if (cudaStreamWaitEvent(s, e.copied, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
+// The schedule entry of this shape with its table copied (or being copied, in order before
+// anything that follows on `s`) to the device; nullptr when there is none: the first call of
+// the shape is under stream capture, the pool is full, or a CUDA call failed. The caller then
+// launches one CTA per item.
+ScheduleEntry* get_schedule(int dev, const Params& p, bool causal, bool splitk, bool f32, int grid, cudaStream_t s) {
   ScheduleKey key{};
   key.dev = dev;
   key.BH = p.BH;
@@ -380,28 +430,47 @@ const int* get_schedule(int dev, const Params& p, bool causal, bool splitk, bool
   key.num_mb = p.num_mb;
   key.num_items = p.num_items;
   key.grid = grid;
-  std::lock_guard<std::mutex> lock(g_schedule_mutex);
-  auto found = g_schedules.find(key);
-  if (found != g_schedules.end()) return found->second;
-  if (dev < 0 || dev >= kMaxDevices) return nullptr;
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
-  SchedulePool& pool = g_schedule_pools[dev];
-  if (pool.base == nullptr && cudaGetSymbolAddress(reinterpret_cast<void**>(&pool.base), g_schedule_pool) != cudaSuccess) {
-    cudaGetLastError();
-    pool.base = nullptr;
-    return nullptr;
+  ScheduleEntry* existing = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_schedule_mutex);
+    auto found = g_schedules.find(key);
+    if (found != g_schedules.end()) {
+      existing = &found->second;  // map nodes are never erased once their copy is enqueued
+    } else {
+      if (dev < 0 || dev >= kMaxDevices || stream_capturing(s)) return nullptr;
+      SchedulePool& pool = g_schedule_pools[dev];
+      if (pool.base == nullptr &&
+          cudaGetSymbolAddress(reinterpret_cast<void**>(&pool.base), g_schedule_pool) != cudaSuccess) {
+        cudaGetLastError();
+        pool.base = nullptr;
+        return nullptr;
+      }
+      std::vector<int> host = build_schedule(p, causal, splitk, f32, grid);
+      if (pool.used + host.size() > kSchedulePoolInts) return nullptr;
+      cudaEvent_t ev = nullptr;
+      if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+      }
+      ScheduleEntry& e = g_schedules[key];
+      e.host = std::move(host);
+      e.table = pool.base + pool.used;
+      e.copied = ev;
+      if (cudaMemcpyAsync(e.table, e.host.data(), e.host.size() * sizeof(int), cudaMemcpyHostToDevice, s) !=
+              cudaSuccess ||
+          cudaEventRecord(ev, s) != cudaSuccess) {
+        cudaGetLastError();
+        cudaStreamSynchronize(s);  // whatever was enqueued has finished before the entry goes away
+        cudaGetLastError();
+        cudaEventDestroy(ev);
+        g_schedules.erase(key);
+        return nullptr;
+      }
+      pool.used += e.host.size();
+      return &e;  // the copy is in order on `s` before the launch that follows
+    }
   }
-  const std::vector<int> host = build_schedule(p, causal, splitk, f32, grid);
-  if (pool.used + host.size() > kSchedulePoolInts) return nullptr;
-  int* d = pool.base + pool.used;
-  if (cudaMemcpy(d, host.data(), host.size() * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  pool.used += host.size();
-  g_schedules[key] = d;
-  return d;
+  return schedule_ready(*existing, s) ? existing : nullptr;
 }
 
 // Shared by fa_forward (splits = 1) and fa_forward_splitkv (splits >= 1 after the automatic
@@ -474,15 +543,27 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   for (int i = 0; i < kCacheSize; ++i) {
     const LaunchEntry& c = t_cache[i];
     if (c.valid && c.key == key) {
+      const Params* pp = &c.params;
+      int grid = c.grid;
+      Params p2;
+      if (c.sched != nullptr && !schedule_ready(*c.sched, s)) {
+        // The table's copy is not known to be complete and this stream cannot wait for it
+        // (stream capture): one CTA per item, without the table.
+        p2 = c.params;
+        p2.schedule = nullptr;
+        pp = &p2;
+        grid = p2.num_items;
+        g_schedule_fallbacks.fetch_add(1, std::memory_order_relaxed);
+      }
       if (c.f32) {
-        e = launch_forward_f32(c.params, c.grid, D, key.causal != 0, s);
+        e = launch_forward_f32(*pp, grid, D, key.causal != 0, s);
       } else if (c.splits > 1) {
-        e = launch_partial(c.params, c.grid, D, bf16, key.causal != 0, s);
+        e = launch_partial(*pp, grid, D, bf16, key.causal != 0, s);
         if (e == cudaSuccess)
           e = launch_merge(c.params.o_part, kPartsF32, c.params.lse_part, c.splits, c.rows, D, c.o, bf16, c.lse,
                            c.num_sms, s);
       } else {
-        e = launch(c.params, c.grid, c.splitk, c.pair, D, bf16, key.causal != 0, s);
+        e = launch(*pp, grid, c.splitk, c.pair, D, bf16, key.causal != 0, s);
       }
       return e == cudaSuccess ? FA_OK : cuda_fail(e);
     }
@@ -523,11 +604,14 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   // split-K launches also take one CTA per SM: CTA c runs items c and 2 grid - 1 - c.
   int grid = (plan.by_dispatch || p.num_items < info->num_sms) ? p.num_items : info->num_sms;
   p.schedule = nullptr;
+  ScheduleEntry* sched = nullptr;
   if (plan.by_dispatch) {
-    const int* sched = get_schedule(dev, p, causal != 0, splitk, f32, info->num_sms, s);
+    sched = get_schedule(dev, p, causal != 0, splitk, f32, info->num_sms, s);
     if (sched != nullptr) {
-      p.schedule = sched;
+      p.schedule = sched->table;
       grid = info->num_sms;
+    } else {
+      g_schedule_fallbacks.fetch_add(1, std::memory_order_relaxed);
     }
   }
 
@@ -544,7 +628,8 @@ int forward_impl(const void* q, const void* k, const void* v, void* o, float* ls
   slot.lse = lse;
   slot.rows = BH * N;
   slot.num_sms = info->num_sms;
-  slot.valid = true;
+  slot.sched = sched;
+  slot.valid = sched != nullptr || !plan.by_dispatch;  // a launch without its table is not cached
   if (f32) {
     e = launch_forward_f32(p, grid, D, causal != 0, s);
   } else if (splits > 1) {
@@ -654,6 +739,19 @@ int fa_debug_work_plan(int B, int H, int N, int D, int causal, int dtype, int nu
     u[5] = U.n1;
   }
   return len;
+}
+
+int fa_schedule_pool_status(size_t* used_bytes, size_t* capacity_bytes, unsigned long long* fallbacks) {
+  if (fallbacks != nullptr) *fallbacks = fa::g_schedule_fallbacks.load(std::memory_order_relaxed);
+  if (capacity_bytes != nullptr) *capacity_bytes = fa::kSchedulePoolInts * sizeof(int);
+  if (used_bytes != nullptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fa::cuda_fail(e);
+    std::lock_guard<std::mutex> lock(fa::g_schedule_mutex);
+    *used_bytes = (dev >= 0 && dev < fa::kMaxDevices) ? fa::g_schedule_pools[dev].used * sizeof(int) : 0;
+  }
+  return FA_OK;
 }
 
 int fa_check_device_status(void) {
@@ -770,9 +868,10 @@ int fa_forward_splitkv_noalloc(const void* q, const void* k, const void* v, void
   }
   int splits = num_splits;
   if (splits == 0) {
+    // The cost model's choice, lowered to the largest count whose partials fit the scratch.
     splits = fa_splitkv_num_splits(B, H, N, D, causal);
     if (splits < 0) return splits;
-    if (splits > 1 && workspace_bytes(BH, N, D, splits) > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
+    while (splits > 1 && workspace_bytes(BH, N, D, splits) > kNoAllocScratchBytes) --splits;
   }
   return forward_impl(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, splits, ptr, kNoAllocScratchBytes, stream);
 }

@@ -65,6 +65,7 @@ SIGNATURES = {
     "fa_splitkv_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_int]),
     "fa_splitkv_num_splits": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "fa_schedule_pool_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "fa_merge_partials": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
@@ -115,6 +116,16 @@ def _check(code: int):
 def check_device_status() -> None:
     """Synchronise the current device and raise FAError if a kernel timed out."""
     _check(load_library().fa_check_device_status())
+
+
+def schedule_pool_status():
+    """(used bytes, capacity bytes) of the current device's work-table pool, and the number of
+    launches in this process that needed a work table but ran without one."""
+    used = ctypes.c_size_t(0)
+    cap = ctypes.c_size_t(0)
+    fb = ctypes.c_ulonglong(0)
+    _check(load_library().fa_schedule_pool_status(ctypes.byref(used), ctypes.byref(cap), ctypes.byref(fb)))
+    return int(used.value), int(cap.value), int(fb.value)
 
 
 def set_watchdog_ns(ns: int) -> None:
