@@ -1,11 +1,14 @@
 """Benchmark of the fused attention forward pass (one JSON line on stdout).
 
 A step is one forward pass (one kernel launch of the C-ABI library) over the
-headline workload: 1B-class LLM prefill attention, B=1, H=32, N=1024, D=64,
-fp16, causal, inputs resident in HBM. The steps cycle through enough copies of
-the inputs (and outputs) that their total is more than twice the 126 MB L2, so
-no step finds its inputs in L2; the K timed steps run back to back on one stream
-between two CUDA events.
+headline workload, the largest single-GPU configuration: long-sequence prefill,
+B=1, H=8, N=16384, D=128, fp16, non-causal, Q and K drawn N(0,1) then scaled by
+4 (exp(m_old - m_new) underflows), V ~ U(-1,1), inputs resident in HBM. The
+steps cycle through enough copies of the inputs (and outputs) that their total
+is more than twice the 126 MB L2, so no step finds its inputs in L2; the K timed
+steps run back to back on one stream between two CUDA events (the mean step
+time); a second pass of K steps with an event between consecutive steps gives
+the median, p10 and p90.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
                     [--workload c1..c5] [--kernel-only] [--no-sweep]
@@ -36,7 +39,7 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd TFLOPS and % of GB300 fp16/bf16 tensor peak; DRAM bytes vs min"
 UNIT = "TFLOP/s"
-HEADLINE = "c2"
+HEADLINE = "c5"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 126 << 20
 # The sources of the fused kernels whose DRAM traffic profiles/fa_fwd_dram_traffic.json records.
@@ -164,9 +167,61 @@ def workload_desc(w):
             "values": "Q,K x%g N(0,1); V %s" % (w.qk_mult, "U(-1,1)" if w.v_uniform else "N(0,1)")}
 
 
+def traffic_fields(w, tr):
+    """Traffic of one launch (ncu summary) against the minimum |Q|+|K|+|V|+|O|.
+
+    traffic = DRAM bytes read + bytes the kernel stored. The stores (O, lse) are counted where
+    they enter L2 (write sectors x 32 B): O of a small workload can still sit in the L2 when the
+    kernel ends, so DRAM write counters taken over the launch alone miss it, but every stored
+    byte is a distinct output byte and reaches DRAM exactly once."""
+    from tiled_attention_prefill_gb300 import workloads
+    eb = 4 if w.dtype == "fp32" else 2
+    qkv = 3 * w.B * w.H * w.N * w.D * eb
+    o = w.B * w.H * w.N * w.D * eb
+    lse = 4 * w.B * w.H * w.N
+    out = {"min_bytes": workloads.min_dram_bytes(w.B, w.H, w.N, w.D, elem_bytes=eb, with_lse=False),
+           "traffic_bytes": None, "traffic_vs_min": None, "read_vs_qkv": None, "stored_vs_o": None}
+    if not tr or tr.get("stored_bytes") is None:
+        return out
+    t = tr["read_bytes"] + tr["stored_bytes"]
+    out.update(traffic_bytes=t, traffic_vs_min=t / out["min_bytes"], traffic_vs_min_with_lse=t / (qkv + o + lse),
+               read_vs_qkv=tr["read_bytes"] / qkv, stored_vs_o=tr["stored_bytes"] / (o + lse),
+               dram_write_in_launch=tr.get("write_bytes"))
+    return out
+
+
+def sample_rows(w, n_heads=4, seed=0):
+    """(b*H + h, i) pairs: tile edges, first and last rows, and random rows of a few heads."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    BH, N = w.B * w.H, w.N
+    heads = sorted(set([0, BH - 1] + rng.integers(0, BH, size=n_heads).tolist()))
+    fixed = [0, 1, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1]
+    rows = []
+    for bh in heads:
+        idx = set(i for i in fixed if 0 <= i < N) | set(rng.integers(0, N, size=24).tolist())
+        rows += [(bh, i) for i in sorted(idx)]
+    return np.array(rows, dtype=np.int64)
+
+
+def sampled_errors(w, rows, go, gl):
+    """Max abs errors of the CUDA path's sampled rows against the oracle on the same rows."""
+    import numpy as np
+
+    import oracle
+    from tiled_attention_prefill_gb300 import workloads
+    q, k, v = workloads.make_qkv(w)
+    ro, rl = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
+    return float(np.abs(go - ro).max()), float(np.abs(gl - rl).max())
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
-def cpu_oracle_rate(w, budget_s: float = 12.0, max_heads=None):
-    """Time the oracle on whole heads of the workload until ~budget_s; returns (TFLOP/s, sample, threads)."""
+def cpu_oracle_rate(w, budget_s: float = 12.0, max_heads=None, gpu_out=None, parity=None):
+    """Time the oracle on whole heads of the workload until ~budget_s; returns (TFLOP/s, sample, threads).
+
+    gpu_out: optional (O [B*H, N, D], lse [B*H, N]) fp64 arrays of the CUDA path on the same
+    inputs; the heads the oracle computed are then compared with them (untimed) and the
+    largest errors are stored in the dict `parity`."""
     import numpy as np
 
     import oracle
@@ -182,8 +237,14 @@ def cpu_oracle_rate(w, budget_s: float = 12.0, max_heads=None):
     while (done_heads < max_heads) if max_heads is not None else (done_heads == 0 or elapsed < budget_s):
         rows = np.stack([np.full(w.N, h % BH), np.arange(w.N)], axis=1)
         t0 = time.perf_counter()
-        oracle.attention_rows(q64, k64, v64, w.scale, w.causal, rows)
+        ro, rl = oracle.attention_rows(q64, k64, v64, w.scale, w.causal, rows)
         elapsed += time.perf_counter() - t0
+        if gpu_out is not None and parity is not None:
+            eo = float(np.abs(gpu_out[0][h % BH] - ro).max())
+            el = float(np.abs(gpu_out[1][h % BH] - rl).max())
+            parity["o_max_abs_err"] = max(parity.get("o_max_abs_err", 0.0), eo)
+            parity["lse_max_abs_err"] = max(parity.get("lse_max_abs_err", 0.0), el)
+            parity["heads_compared"] = parity.get("heads_compared", 0) + 1
         done_heads += 1
         h += 1
     rate = per_head * done_heads / elapsed / 1e12
@@ -192,37 +253,65 @@ def cpu_oracle_rate(w, budget_s: float = 12.0, max_heads=None):
 
 
 def run_reference(args, w):
+    """The reference arm: the fp64 oracle on the host cores, one bounded sample per step.
+
+    A step is a block of `rows_per_step` consecutive query rows of one head (the blocks cycle
+    through the heads and row ranges of the workload); its FLOPs are counted exactly (4*D per
+    unmasked (query, key) pair)."""
     world, rank, _ = dist_setup(want_gpu=False)
     if rank != 0:
         return 0
+    import numpy as np
+
     import oracle
+    from tiled_attention_prefill_gb300 import workloads
     oracle.build()
-    heads_per_step = 2
-    for _ in range(args.warmup):
-        cpu_oracle_rate(w, budget_s=0.0, max_heads=1)
-    rates, times = [], []
-    for _ in range(args.steps):
-        r, sample, threads, el = cpu_oracle_rate(w, budget_s=0.0, max_heads=heads_per_step)
-        rates.append(r)
-        times.append(el)
-    value = statistics.mean(rates)
-    flops_step = heads_per_step * (4.0 * w.N * w.N * w.D / (2 if w.causal else 1))
+    rows_per_step = min(w.N, 2048)
+    q, k, v = workloads.make_qkv(w)
+    q64, k64, v64 = (oracle.to_f64(x) for x in (q, k, v))
+    BH = w.B * w.H
+    blocks = [(bh, r0) for bh in range(BH) for r0 in range(0, w.N, rows_per_step)]
+
+    def step(i):
+        bh, r0 = blocks[i % len(blocks)]
+        idx = np.arange(r0, min(r0 + rows_per_step, w.N))
+        rows = np.stack([np.full(len(idx), bh), idx], axis=1)
+        keys = (idx + 1).sum() if w.causal else len(idx) * w.N
+        t0 = time.perf_counter()
+        oracle.attention_rows(q64, k64, v64, w.scale, w.causal, rows)
+        return time.perf_counter() - t0, 4.0 * w.D * float(keys)
+
+    for i in range(args.warmup):
+        step(i)
+    times, flops = [], []
+    for i in range(args.steps):
+        t, f = step(args.warmup + i)
+        times.append(t)
+        flops.append(f)
+    value = sum(flops) / sum(times) / 1e12
     # n_gpus is the launch's N (the same as the GPU arm's line); the work runs on rank 0's host cores
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_desc(w),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": "%d heads per step of workload %s (fp64 oracle, %.3g FLOP per step)"
-                                       % (heads_per_step, w.name, flops_step)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": "%d consecutive query rows of one head per step of workload %s (fp64 "
+                                       "oracle, %.3g FLOP per step on average)"
+                                       % (rows_per_step, w.name, statistics.mean(flops))},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def time_steps(fwd, steps, warmup, stream):
-    """Mean CUDA-event time (ms) of one step over `steps` back-to-back calls fwd(i) on `stream`."""
+def time_steps(fwd, steps, warmup, stream, per_step=None):
+    """Mean CUDA-event time (ms) of one step over `steps` back-to-back calls fwd(i) on `stream`.
+
+    The timed region has one event before the first step and one after the last, so
+    consecutive launches keep their overlap (programmatic dependent launch). If `per_step` is a
+    list, a second pass of `steps` calls follows with an event between consecutive steps, and
+    its step times (ms) are appended to it: an event between two launches removes that
+    overlap, so these times are for the distribution (median, p10, p90), not the mean."""
     import torch
     for i in range(warmup):
         fwd(i)
@@ -237,7 +326,31 @@ def time_steps(fwd, steps, warmup, stream):
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
-    return start.elapsed_time(end) / steps
+    ms = start.elapsed_time(end) / steps
+    if per_step is not None:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        evs[0].record(stream)
+        for i in range(steps):
+            fwd(warmup + steps + i)
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        per_step.extend(evs[i].elapsed_time(evs[i + 1]) for i in range(steps))
+    return ms
+
+
+def step_stats(per_step):
+    """Median, p10 and p90 (ms) of the step times."""
+    xs = sorted(per_step)
+    if not xs:
+        return None
+
+    def pct(p):
+        i = p * (len(xs) - 1)
+        lo = int(i)
+        hi = min(lo + 1, len(xs) - 1)
+        return xs[lo] + (xs[hi] - xs[lo]) * (i - lo)
+    return {"median_ms": pct(0.5), "p10_ms": pct(0.1), "p90_ms": pct(0.9), "n": len(xs),
+            "method": "a second pass of the same steps with a CUDA event between consecutive steps"}
 
 
 def n_copies(bytes_per_set: int, cap_bytes: int = 4 << 30) -> int:
@@ -264,12 +377,16 @@ def run_fa(args, w):
     peak_of = {"fp16": peak_tf, "bf16": peak_tf, "fp32": peak_tf * 1.1 / 2.25}
     copies_used = {}
 
-    def measure(wl, steps, warmup, splits=None, naive=False):
+    def measure(wl, steps, warmup, splits=None, naive=False, per_step=None, rows=None, outputs=None):
         """Mean step time (ms) with the inputs cycled over enough copies to defeat L2.
 
         splits: None times fa_forward; an integer times fa_forward_splitkv with that many
         splits (one workspace, reused by every step in stream order). naive: times the
-        unfused baseline fa_naive_forward (its S/P workspace reused likewise)."""
+        unfused baseline fa_naive_forward (its S/P workspace reused likewise). per_step: a
+        list that receives the step times. After the timed steps, one more (untimed) call on
+        the first input set; `rows` (an int64 array of (b*H + h, i) pairs) selects output rows
+        of it returned as fp64 host arrays (O [R, D], lse [R]) in outputs["rows"], and
+        outputs["full"] receives the whole result (O [B*H, N, D], lse [B*H, N]) when present."""
         q0, k0, v0 = workloads.make_qkv(wl)
         set_bytes = 4 * q0.numel() * q0.element_size() + wl.B * wl.H * wl.N * 4
         n = n_copies(set_bytes)
@@ -296,8 +413,19 @@ def run_fa(args, w):
                 fa.forward_splitkv(q, k, v, causal=wl.causal, scale=wl.scale, num_splits=splits, workspace=ws,
                                    out=o, lse=lse)
 
-        ms = time_steps(fwd, steps, warmup, stream)
+        ms = time_steps(fwd, steps, warmup, stream, per_step)
         fa.check_device_status()
+        if outputs is not None:
+            fwd(0)
+            torch.cuda.synchronize()
+            o_all = sets[0][3].reshape(wl.B * wl.H, wl.N, wl.D)
+            l_all = sets[0][4].reshape(wl.B * wl.H, wl.N)
+            if rows is not None:
+                ri = torch.as_tensor(rows, device=dev)
+                outputs["rows"] = (o_all[ri[:, 0], ri[:, 1]].double().cpu().numpy(),
+                                   l_all[ri[:, 0], ri[:, 1]].double().cpu().numpy())
+            if "full" in outputs:
+                outputs["full"] = (o_all.double().cpu().numpy(), l_all.double().cpu().numpy())
         flops = workloads.attention_flops(wl.B, wl.H, wl.N, wl.D, wl.causal)
         del sets, ws
         return ms, flops
@@ -317,12 +445,15 @@ def run_fa(args, w):
     sampler = ClockSampler(local) if not args.kernel_only else None
     if sampler:
         sampler.start()
+    per_step = []
+    head_out = {}
     if args.kernel_only and args.path != "fused":
         # the split-KV (automatic split count) or the naive path alone, for ncu captures
         splits = fa.splitkv_num_splits(w.B, w.H, w.N, w.D, w.causal) if args.path == "splitkv" else None
         ms_local, flops = measure(w, args.steps, args.warmup, splits=splits, naive=args.path == "naive")
     else:
-        ms_local, flops = measure(w, args.steps, args.warmup)
+        head_out = {} if args.kernel_only or args.no_cpu else {"full": None}
+        ms_local, flops = measure(w, args.steps, args.warmup, per_step=per_step, outputs=head_out)
     ms = max_over_ranks(ms_local)
     value = world * flops / (ms * 1e-3) / 1e12
     if args.kernel_only:
@@ -395,18 +526,21 @@ def run_fa(args, w):
     d2h = out_h[0].numel()
 
     sweep = {}
+    sweep_rows = {}  # workload -> (sampled rows, GPU O rows, GPU lse rows), for the oracle leg
     if not args.no_sweep:
         for name, wl in workloads.WORKLOADS.items():
             st = 50 if wl.N <= 4096 else 20
-            m, f = measure(wl, st, 3)
+            steps_ms = []
+            rows = sample_rows(wl) if not args.no_cpu else None
+            outs = {} if rows is not None else None
+            m, f = measure(wl, st, 3, per_step=steps_ms, rows=rows, outputs=outs)
+            if rows is not None:
+                sweep_rows[name] = (rows,) + outs["rows"]
             tf = f / (m * 1e-3) / 1e12
-            tr = measured_traffic(name)
-            sweep[name] = {"ms_mean": m, "tflops": tf, "frac_of_peak": tf / peak_of[wl.dtype],
-                           "peak_tflops": peak_of[wl.dtype], "input_copies": copies_used[name][0],
-                           "dram_bytes": tr["dram_bytes"] if tr else None,
-                           "dram_vs_min": (tr["dram_bytes"] / workloads.min_dram_bytes(
-                               wl.B, wl.H, wl.N, wl.D, elem_bytes=4 if wl.dtype == "fp32" else 2, with_lse=False))
-                           if tr else None}
+            sweep[name] = {"ms_mean": m, "step_ms": step_stats(steps_ms), "tflops": tf,
+                           "frac_of_peak": tf / peak_of[wl.dtype], "peak_tflops": peak_of[wl.dtype],
+                           "input_copies": copies_used[name][0]}
+            sweep[name].update(traffic_fields(wl, measured_traffic(name)))
             # the unfused baseline (S and P in memory) on the fp16 workloads whose S fits in 1 GiB
             if wl.dtype == "fp16" and wl.B * wl.H * wl.N * wl.N * 2 <= (1 << 30):
                 m3, _ = measure(wl, st, 3, naive=True)
@@ -427,25 +561,32 @@ def run_fa(args, w):
 
     if rank != 0:
         return 0
-    from tiled_attention_prefill_gb300 import workloads as W
     achieved = flops / (ms_local * 1e-3) / 1e12
-    tr = measured_traffic(w.name)
-    min_bytes = W.min_dram_bytes(w.B, w.H, w.N, w.D, with_lse=False)
+    tf_fields = traffic_fields(w, measured_traffic(w.name))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": dict(workload_desc(w),
                        l2="inputs larger than L2: steps cycle over %d copies of q/k/v/o/lse (%.0f MiB in total, "
-                          "> 2 x 126 MB L2); timed steps back to back between two CUDA events"
+                          "> 2 x 126 MB L2); timed steps back to back on one stream between two CUDA events"
                           % (copies_used[w.name][0], copies_used[w.name][1] / 2**20),
                        parallelism="replicas" if world > 1 else "single GPU"),
+        "step_ms": step_stats(per_step),
         "pct_of_peak": 100.0 * achieved / peak_tf,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "peak_source": "%s bf16_tflops (burst; fp16 dense rate equal)" % peak_kind,
-                     "traffic": tr["dram_bytes"] if tr else None,
-                     "traffic_vs_min": (tr["dram_bytes"] / min_bytes) if tr else None,
-                     "min_bytes": min_bytes},
+                     "frac": achieved / peak_tf,
+                     "peak_source": "%s bf16_tflops (burst: the kernel is timed alone; fp16 dense rate equal)"
+                                    % peak_kind,
+                     "peak_sustained": peak_sus, "frac_of_sustained": achieved / peak_sus,
+                     "traffic": tf_fields["traffic_bytes"],
+                     "traffic_vs_min": tf_fields["traffic_vs_min"],
+                     "read_vs_qkv": tf_fields["read_vs_qkv"], "stored_vs_o": tf_fields["stored_vs_o"],
+                     "min_bytes": tf_fields["min_bytes"],
+                     "traffic_def": "ncu, one launch: dram__bytes_read.sum + bytes the kernel stored "
+                                    "(lts__t_sectors_op_write.sum x 32; O and lse, every byte of which reaches "
+                                    "DRAM once, whether before or after the kernel ends)"},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "method": "every step copies its q, k, v in (one pinned H2D copy) and o, lse out (one D2H "
@@ -457,9 +598,18 @@ def run_fa(args, w):
     if sweep:
         line["workloads"] = sweep
     if not args.no_cpu and world >= 1:
-        rate, sample, threads, el = cpu_oracle_rate(w)
+        # The oracle leg: the oracle timed on whole heads of the headline workload (the CPU
+        # baseline); untimed, the same heads and sampled rows of every swept workload are
+        # compared with the CUDA path's outputs (max abs errors).
+        par = {}
+        rate, sample, threads, el = cpu_oracle_rate(w, gpu_out=head_out.get("full"), parity=par)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
                                 "seconds": el}
+        line["max_abs_err"] = dict(par, tol_o=2e-3 if w.dtype == "fp16" else 1e-2, tol_lse=1e-3,
+                                   what="whole heads the oracle computed for the CPU baseline")
+        for name, (rows, go, gl) in sweep_rows.items():
+            eo, el_ = sampled_errors(workloads.WORKLOADS[name], rows, go, gl)
+            sweep[name]["max_abs_err"] = {"o": eo, "lse": el_, "rows_compared": int(len(rows))}
     print(json.dumps(line), flush=True)
     return 0
 

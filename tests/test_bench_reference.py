@@ -26,10 +26,11 @@ def test_reference_arm_json_line():
         assert key in d, key
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] >= 3
     assert d["higher_is_better"] is True and d["vs_baseline"] is None and d["dtype"] == "f64"
-    assert d["config"]["workload"].startswith("c2:")
+    assert d["config"]["workload"].startswith("c5:")
     assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"] and d["e2e"]["value"] == d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
-    # the rate is the step's FLOP count over the step's time: two causal heads of c2
-    flops_step = 2 * 4.0 * d["config"]["N"] ** 2 * d["config"]["D"] / 2
+    # the rate is the step's FLOP count over the step's time: 2048 query rows of a non-causal
+    # c5 head, each against all N keys
+    flops_step = 4.0 * 2048 * d["config"]["N"] * d["config"]["D"]
     assert abs(flops_step / (d["ms_per_step"] * 1e-3) / 1e12 - d["value"]) <= 0.02 * d["value"]
