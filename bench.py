@@ -585,8 +585,8 @@ def run_fa(args, w):
                      "read_vs_qkv": tf_fields["read_vs_qkv"], "stored_vs_o": tf_fields["stored_vs_o"],
                      "min_bytes": tf_fields["min_bytes"],
                      "traffic_def": "ncu, one launch: dram__bytes_read.sum + bytes the kernel stored "
-                                    "(lts__t_sectors_op_write.sum x 32; O and lse, every byte of which reaches "
-                                    "DRAM once, whether before or after the kernel ends)"},
+                                    "(lts__t_sectors_srcunit_tex_op_write.sum x 32: O and lse, every byte of which "
+                                    "reaches DRAM once, whether before or after the kernel ends)"},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "method": "every step copies its q, k, v in (one pinned H2D copy) and o, lse out (one D2H "
