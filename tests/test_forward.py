@@ -101,7 +101,7 @@ def test_workload_both_decompositions(name, decomposition):
     assert_close(o, lse, ro, rl, w.dtype, name + " " + decomposition)
 
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c3c", "c4", "c5", "p2s512", "p2s1024"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c3c", "c4", "c5", "p2s512", "p2s1024", "lc1"])
 def test_workload_full_oracle(name):
     """Every output element of each workload against the oracle, the full-size ones included.
 

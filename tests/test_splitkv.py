@@ -109,19 +109,14 @@ def test_splitkv_workloads_full_oracle(name, splits):
 
 
 @pytest.mark.parametrize("splits", [0, 4])
-def test_splitkv_long_causal_sampled_rows(splits):
-    """One long causal sequence (the split-KV target case): sampled rows against the oracle."""
+def test_splitkv_long_causal_full_oracle(splits):
+    """One long causal sequence (the split-KV target case, 16384 tokens): every element against
+    the oracle (~34 GFLOP of fp64 on the host cores)."""
     w = workloads.WORKLOADS["lc1"]
     q, k, v = workloads.make_qkv(w)
     o, lse = run_splitkv(q, k, v, w.causal, w.scale, splits)
-    assert np.isfinite(o).all() and np.isfinite(lse).all()
-    rng = np.random.default_rng(3)
-    N = w.N
-    idx = sorted(set([0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 2, N - 1] +
-                     rng.integers(0, N, size=60).tolist()))
-    rows = np.array([(0, i) for i in idx])
-    ro, rl = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
-    assert_close(o.reshape(-1, N, w.D)[0, idx], lse.reshape(-1, N)[0, idx], ro, rl, w.dtype, "lc1")
+    ro, rl = oracle.attention(q, k, v, w.scale, w.causal)
+    assert_close(o, lse, ro, rl, w.dtype, "lc1 splits=%d" % splits)
 
 
 def test_one_split_is_the_fused_forward():
