@@ -179,3 +179,63 @@ def test_runs_on_a_side_stream():
     s.synchronize()
     ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), w.scale, False)
     assert_close(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ro, rl, "fp16")
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_extreme_score_range(dtype, D, causal):
+    """Q and K scaled by 16 (scores of a few hundred): the row max jumps by far more than the
+    deferred-rescale threshold between tiles, and almost every P underflows to zero, so most
+    rows attend to one or a few keys. Ragged N, several tiles, single-query-tile items.
+
+    Tolerance from the arithmetic (these are not the five configurations the stated
+    tolerances are for): P is rounded to the 16-bit type with relative error <= u (2^-8 for
+    bf16, 2^-11 for fp16). The running max can trail the row max by up to 2^8, so even the
+    dominant key's p is rounded, while l sums the unrounded p: O_i is off by at most
+    u * max_j |v_j| from that, plus u * |O_i| from rounding the output; fp32 scores and sums
+    add less than 1e-5 here (the scaled scores' fp32 error is ~2e-4, and they enter O only
+    through the exponentials of the few largest). lse: 1e-3 as for the configurations (its
+    fp32 error is ~4e-4 at these magnitudes)."""
+    w = workloads.Workload("x16", 1, 4, 700, D, dtype, causal, seed=91 + D, qk_mult=16.0)
+    q, k, v = workloads.make_qkv(w)
+    o, lse = run_cuda(q, k, v, causal, w.scale)
+    ro, rl = oracle.attention(q, k, v, w.scale, causal)
+    u = {"fp16": 2.0 ** -11, "bf16": 2.0 ** -8}[dtype]
+    vmax = np.abs(v.double().numpy()).max(axis=2, keepdims=True)  # per head and feature
+    bound = u * (vmax + np.abs(ro)) + 1e-5
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    ratio = np.abs(o - ro) / bound
+    i = np.unravel_index(np.argmax(ratio), ratio.shape)
+    assert ratio.max() <= 1.0, "O x16: error %.3e at %s, bound %.3e" % (abs(o[i] - ro[i]), i, bound[i])
+    assert np.abs(lse - rl).max() <= TOL_LSE
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_explicit_scale(D):
+    """A scale other than 1/sqrt(D) reaches the kernel (it is folded with log2 e there)."""
+    w = workloads.Workload("scl", 2, 3, 333, D, "fp16", True, seed=17 + D)
+    q, k, v = workloads.make_qkv(w)
+    for scale in (0.05, 0.3):
+        o, lse = run_cuda(q, k, v, True, scale)
+        ro, rl = oracle.attention(q, k, v, scale, True)
+        assert_close(o, lse, ro, rl, "fp16", "scale %g" % scale)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_zero_queries_give_the_mean_of_v(D, causal):
+    """Q = 0: every score is 0, so O_i is the mean of V over J(i) and lse_i = ln |J(i)|."""
+    w = workloads.Workload("q0", 1, 2, 520, D, "fp16", causal, seed=5 + D)
+    q, k, v = workloads.make_qkv(w)
+    q = torch.zeros_like(q)
+    o, lse = run_cuda(q, k, v, causal, w.scale)
+    v64 = v.double().numpy()
+    n = np.arange(1, w.N + 1, dtype=np.float64)
+    if causal:
+        ro = np.cumsum(v64, axis=2) / n[None, None, :, None]
+        rl = np.broadcast_to(np.log(n), lse.shape)
+    else:
+        ro = np.broadcast_to(v64.mean(axis=2, keepdims=True), v64.shape)
+        rl = np.full(lse.shape, np.log(w.N))
+    assert_close(o, lse, ro, rl, "fp16", "Q = 0")
