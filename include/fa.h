@@ -311,6 +311,15 @@ FA_API int fa_debug_work_plan(int B, int H, int N, int D, int causal, int dtype,
                               int capacity);
 
 /*
+ * Inspection hook for the split count (host only, no CUDA call) on a GPU with num_sms SMs:
+ * the count fa_splitkv_num_splits gives for this shape (for_noalloc 0), or the count
+ * fa_forward_splitkv_noalloc runs with num_splits 0 (for_noalloc 1: that count lowered to the
+ * largest whose partials fit the 32 MiB scratch, down to 1). Returns the count (>= 1),
+ * FA_ERR_INVALID_ARG for bad sizes or num_sms < 1, FA_ERR_UNSUPPORTED for D.
+ */
+FA_API int fa_debug_num_splits(int B, int H, int N, int D, int causal, int num_sms, int for_noalloc);
+
+/*
  * The per-device pool of work tables that causal multi-wave launches use (fa_forward). Host
  * only; the one CUDA call is cudaGetDevice (for used_bytes).
  *   used_bytes, capacity_bytes  (either may be NULL) bytes of the current device's 4 MB pool

@@ -802,6 +802,16 @@ size_t fa_splitkv_workspace_bytes(int B, int H, int N, int D, int num_splits) {
   return fa::workspace_bytes(static_cast<long long>(B) * H, N, D, num_splits);
 }
 
+int fa_debug_num_splits(int B, int H, int N, int D, int causal, int num_sms, int for_noalloc) {
+  if (B < 1 || H < 1 || N < 1 || num_sms < 1) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  int splits = fa::choose_splits(BH, N, D, causal != 0, num_sms);
+  if (for_noalloc)
+    while (splits > 1 && fa::workspace_bytes(BH, N, D, splits) > fa::kNoAllocScratchBytes) --splits;
+  return splits;
+}
+
 int fa_splitkv_num_splits(int B, int H, int N, int D, int causal) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;

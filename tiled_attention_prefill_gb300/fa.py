@@ -48,6 +48,7 @@ SIGNATURES = {
     "fa_debug_force_stall": (ctypes.c_int, [ctypes.c_int]),
     "fa_debug_work_schedule": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_int]),
     "fa_debug_work_plan": (ctypes.c_int, [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]),
+    "fa_debug_num_splits": (ctypes.c_int, [ctypes.c_int] * 7),
     "fa_forward_splitkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
@@ -368,6 +369,16 @@ def naive_forward(q, k, v, causal: bool = False, scale: float | None = None, wor
         raise FAError(rc, error_string(rc) + " (cublasStatus %d)" % load_library().fa_naive_last_library_error())
     _check(rc)
     return out, lse
+
+
+def debug_num_splits(B: int, H: int, N: int, D: int, causal: bool, num_sms: int, noalloc: bool = False) -> int:
+    """The split count ``splitkv_num_splits`` gives for this shape on ``num_sms`` SMs, or with
+    ``noalloc`` the one ``forward_splitkv_noalloc`` runs with ``num_splits=0`` (host only)."""
+    n = load_library().fa_debug_num_splits(int(B), int(H), int(N), int(D), int(bool(causal)), int(num_sms),
+                                           int(bool(noalloc)))
+    if n < 0:
+        _check(n)
+    return n
 
 
 def debug_work_plan(B: int, H: int, N: int, D: int, causal: bool, dtype: int, num_sms: int):
