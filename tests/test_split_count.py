@@ -10,10 +10,7 @@ SCRATCH = fa.NOALLOC_SCRATCH_BYTES
 
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
-    try:
-        fa.load_library()
-    except Exception as exc:  # the library is built by __graft_entry__.build()
-        pytest.skip("library not built: %s" % exc)
+    return fa.load_library()  # built by __graft_entry__.build(); a missing library fails the test
 
 
 # (B, H, N, D, causal) -> the count chosen on 152 SMs. Each was timed on a GB300 against every
