@@ -617,8 +617,11 @@ def run_fa(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
-    ap.add_argument("--warmup", type=int, default=10)
+    # 20 timed steps of the 0.7 ms headline forward (14 ms): the burst regime the kernel-alone peak
+    # is measured in. Runs of several hundred steps settle under the power cap (sw_power_cap) about
+    # 5% slower; the line reports the fraction of both the burst and the sustained peak.
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["fa", "reference"], default="fa")
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--kernel-only", action="store_true")
