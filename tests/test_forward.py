@@ -239,3 +239,19 @@ def test_zero_queries_give_the_mean_of_v(D, causal):
         ro = np.broadcast_to(v64.mean(axis=2, keepdims=True), v64.shape)
         rl = np.full(lse.shape, np.log(w.N))
     assert_close(o, lse, ro, rl, "fp16", "Q = 0")
+
+
+@pytest.mark.parametrize("shape", [(0, 2, 128, 64), (1, 0, 256, 128), (2, 3, 0, 64)])
+def test_empty_batch_gives_empty_outputs(shape):
+    """No query rows (B, H or N is 0): empty O and lse of the right shapes, from every forward."""
+    for dt in (torch.float16, torch.bfloat16, torch.float32):
+        x = torch.empty(shape, dtype=dt, device="cuda")
+        o, lse = fa.forward(x, x, x, causal=True)
+        assert o.shape == shape and o.dtype == dt and lse.shape == shape[:3] and lse.dtype == torch.float32
+    x = torch.empty(shape, dtype=torch.float16, device="cuda")
+    for f in (fa.forward_splitkv, fa.forward_splitkv_noalloc):
+        o, lse = f(x, x, x, causal=False)
+        assert o.shape == shape and lse.shape == shape[:3]
+    bad = torch.empty(shape[:3] + (96,), dtype=torch.float16, device="cuda")
+    with pytest.raises(fa.FAError):
+        fa.forward(bad, bad, bad)  # the head size is still checked

@@ -180,7 +180,8 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     tensor cores; contiguous).
 
     Returns (o, lse) with o like q and lse [B, H, N] fp32 (lse is None when
-    ``return_lse`` is False and no buffer was given). Runs on the current stream.
+    ``return_lse`` is False and no buffer was given). Runs on the current stream. A batch with
+    no query rows (B, H or N is 0) returns empty outputs without a launch.
     """
     import torch
 
@@ -205,6 +206,8 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     if lse is not None and (lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous()
                             or lse.get_device() != dev):
         raise ValueError("lse must be a contiguous fp32 tensor [B, H, N]")
+    if _empty(q):
+        return out, lse
     dtype = {torch.float16: FA_DTYPE_FP16, torch.bfloat16: FA_DTYPE_BF16, torch.float32: FA_DTYPE_FP32}[q.dtype]
     sc = -1.0 if scale is None else float(scale)
     lib = _lib if _lib is not None else load_library()
@@ -219,6 +222,16 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     if rc != FA_OK:
         _check(rc)
     return out, lse
+
+
+def _empty(q) -> bool:
+    """True for a batch with no query rows (B, H or N is 0), after D is checked: the result is
+    empty, and the C entry points, which take sizes >= 1, are not called."""
+    if q.numel() != 0:
+        return False
+    if q.shape[3] not in (64, 128):
+        _check(FA_ERR_UNSUPPORTED)
+    return True
 
 
 def _check_qkv(torch, q, k, v):
@@ -263,6 +276,8 @@ def forward_splitkv(q, k, v, causal: bool = False, scale: float | None = None, n
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if _empty(q):
+        return out, lse
     with torch.cuda.device(dev):
         splits = num_splits if num_splits > 0 else splitkv_num_splits(B, H, N, D, causal)
         if workspace is None:
@@ -326,6 +341,8 @@ def forward_splitkv_noalloc(q, k, v, causal: bool = False, scale: float | None =
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if _empty(q):
+        return out, lse
     dtype = FA_DTYPE_BF16 if q.dtype == torch.bfloat16 else FA_DTYPE_FP16
     sc = -1.0 if scale is None else float(scale)
     with torch.cuda.device(dev):
