@@ -423,11 +423,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // The producer decodes its first unit now, during setup: the decode reads only the kernel
+  // parameters and the work table (copied before the launch, in stream order), and its
+  // first-touch latency (0.3-0.7 us) was on the path to the first Q load (c2 12.7 -> 12.4 us).
+  Unit u_first{};
+  bool u_first_ok = false;
   if (warp == kLoadWarp && lane == 0) {
     prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
     prefetch_tmap(&p.tm_o);
+    u_first_ok = decode_unit<CAUSAL, SPLITK, PARTIAL, PAIR>(0, p, u_first);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_holder), kTmemCols);
@@ -466,7 +472,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           return true;
         };
         for (int k = 0; ok; ++k) {
-          if (!decode_unit<CAUSAL, SPLITK, PARTIAL, PAIR>(k, p, U)) break;
+          if (k == 0) {
+            if (!u_first_ok) break;
+            U = u_first;
+          } else if (!decode_unit<CAUSAL, SPLITK, PARTIAL, PAIR>(k, p, U)) {
+            break;
+          }
           const int nk = U.nk;
           if (nk == 0) continue;  // empty split-KV range: nothing to load
           // Q tiles: wait until every S MMA of the previous item has read them.

@@ -175,11 +175,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_f32_kernel(const __grid
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // The producer decodes its first item during setup (parameters and work table only), off the
+  // path to the first Q load.
+  const int t_first = (warp == kLoadWarp && lane == 0) ? item_of(0, p) : -1;
+  Item it_first{};
+  int nk_first = 0, n0_first = 0, n1_first = 0;
   if (warp == kLoadWarp && lane == 0) {
     prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
     prefetch_tmap(&p.tm_o);
+    if (t_first >= 0) {
+      it_first = decode_item<CAUSAL>(t_first, p);
+      tile_counts_f32<CAUSAL>(it_first.mb, p.N, nk_first, n0_first, n1_first);
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_holder), L::kTmemCols);
@@ -212,11 +221,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_f32_kernel(const __grid
           return true;
         };
         for (int k = 0; ok; ++k) {
-          const int t = item_of(k, p);
+          const int t = k == 0 ? t_first : item_of(k, p);
           if (t < 0) break;
-          const Item it = decode_item<CAUSAL>(t, p);
-          int nk, n0, n1;
-          tile_counts_f32<CAUSAL>(it.mb, p.N, nk, n0, n1);
+          const Item it = k == 0 ? it_first : decode_item<CAUSAL>(t, p);
+          int nk = nk_first, n0 = n0_first, n1 = n1_first;
+          if (k > 0) tile_counts_f32<CAUSAL>(it.mb, p.N, nk, n0, n1);
           if (!(ok = wait_phase(bar(L::kQEmpty), (q_loads & 1) ^ 1, watch, 0))) break;
           mbar_arrive_expect_tx(bar(L::kQFull), L::kQBytes);
           for (int c = 0; c < L::kChunks; ++c)
