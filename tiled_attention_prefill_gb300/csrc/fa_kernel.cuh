@@ -399,7 +399,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   const Watch watch{abort_flag, p.status, p.timeout_ns};
 
-  if (threadIdx.x == 0) {
+  // Q tiles of unit Uq into the Q buffers (two query tiles of one item, or, paired, a's then b's).
+  auto load_q = [&](const Unit& Uq) {
+    const int nq = (SPLITK ? Uq.nb > 0 : Uq.n1 > 0) ? 2 : 1;
+    mbar_arrive_expect_tx(bar(L::kQFull), nq * L::kTileBytes);
+    for (int i = 0; i < nq; ++i) {
+      const Item& qi = (SPLITK && i > 0) ? Uq.b : Uq.a;
+      const int row0 = SPLITK ? qi.mb * kBM : qi.mb * kItemRows + i * kBM;
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_load_3d(q_addr(i) + c * L::kChunkBytes, &p.tm_q, bar(L::kQFull), c * 64, row0, qi.bh);
+    }
+  };
+  // Setup. The producer lane initialises the barriers, decodes its first work unit (kernel
+  // parameters and the work table, copied before the launch in stream order) and, once the
+  // previous kernel on the stream is done, loads that unit's Q tiles, all before the CTA-wide
+  // barrier: the first load leaves while the other warps set up.
+  Unit u_first{};
+  bool u_first_ok = false, q_first = false;
+  if (warp == kLoadWarp && lane == 0) {
     mbar_init(bar(L::kQFull), 1);
     mbar_init(bar(L::kQEmpty), kMmaIssuers);  // one arrival per MMA warp
     for (int s = 0; s < L::kStages; ++s) {
@@ -422,18 +439,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
     mbar_init(bar(L::kDrain + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  // The producer decodes its first unit now, during setup: the decode reads only the kernel
-  // parameters and the work table (copied before the launch, in stream order), and its
-  // first-touch latency (0.3-0.7 us) was on the path to the first Q load (c2 12.7 -> 12.4 us).
-  Unit u_first{};
-  bool u_first_ok = false;
-  if (warp == kLoadWarp && lane == 0) {
     prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
     prefetch_tmap(&p.tm_o);
     u_first_ok = decode_unit<CAUSAL, SPLITK, PARTIAL, PAIR>(0, p, u_first);
+    if (u_first_ok && u_first.nk > 0) {
+      grid_dependency_wait();  // the inputs may be written by the previous kernel on the stream
+      load_q(u_first);         // fresh Q buffers: no wait for an earlier reader
+      q_first = true;
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_holder), kTmemCols);
@@ -480,16 +495,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) fa_fwd_kernel(const __grid_con
           }
           const int nk = U.nk;
           if (nk == 0) continue;  // empty split-KV range: nothing to load
-          // Q tiles: wait until every S MMA of the previous item has read them.
-          if (!(ok = wait_phase(bar(L::kQEmpty), (q_loads & 1) ^ 1, watch, 0))) break;
-          const int nq = (SPLITK ? U.nb > 0 : U.n1 > 0) ? 2 : 1;
-          mbar_arrive_expect_tx(bar(L::kQFull), nq * L::kTileBytes);
-          for (int i = 0; i < nq; ++i) {
-            // two query tiles of one item, or (paired) a's query tile, then b's
-            const Item& qi = (SPLITK && i > 0) ? U.b : U.a;
-            const int row0 = SPLITK ? qi.mb * kBM : qi.mb * kItemRows + i * kBM;
-            for (int c = 0; c < L::kChunks; ++c)
-              tma_load_3d(q_addr(i) + c * L::kChunkBytes, &p.tm_q, bar(L::kQFull), c * 64, row0, qi.bh);
+          if (!(k == 0 && q_first)) {  // the first unit's Q tiles left during setup
+            // Q tiles: wait until every S MMA of the previous item has read them.
+            if (!(ok = wait_phase(bar(L::kQEmpty), (q_loads & 1) ^ 1, watch, 0))) break;
+            load_q(U);
           }
           ++q_loads;
           // K/V in the MMA warp's consumption order:
