@@ -16,7 +16,8 @@
 //       warps 4-7   softmax warpgroup 1
 //       warp  8     tcgen05 MMA issuer (warp-uniform, one elected lane issues) and TMEM owner;
 //                   at D = 64 with two query tiles per item it issues for warpgroup 0 only
-//       warp  9     TMA producer (one thread)
+//       warp  9     TMA producer (one thread; during setup it also initialises the barriers
+//                   and issues the first work unit's Q load)
 //       warp 10     at D = 64 with two query tiles per item: MMA issuer for warpgroup 1
 //       warps 10-11 otherwise idle
 //     At D = 128, setmaxnreg moves registers from the third warpgroup (88 each) to the softmax
@@ -27,9 +28,10 @@
 //     items leave the second Q tile free, and the ring starts there, one stage deeper; at
 //     D = 128 two-query-tile items stage O one 64-column chunk at a time for a fourth stage.
 //   * S = Q K^T for a warpgroup goes to its own 128 TMEM columns (fp32). The warpgroup reads
-//     its row of S (tcgen05.ld), writes P as fp16/bf16 back into the same columns, and the MMA
-//     warp computes O += P V with P read from TMEM. O (fp32, D columns per warpgroup) stays in
-//     TMEM for the whole K/V loop.
+//     its row of S (tcgen05.ld), writes P as fp16/bf16 into TMEM (at D = 128 over S's columns;
+//     at D = 64 into 64 columns of its own, so that the next S can be computed while the
+//     softmax runs), and the MMA warp computes O += P V with P read from TMEM. O (fp32, D
+//     columns per warpgroup) stays in TMEM for the whole K/V loop.
 //   * Two work decompositions (template SPLITK):
 //       false: a work item is 256 query rows = two 128-row query tiles, one per warpgroup,
 //              sharing every K/V tile loaded (half the K/V traffic per query row).
